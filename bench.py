@@ -1,0 +1,505 @@
+#!/usr/bin/env python3
+"""Benchmark of one paged decode step on GB300.
+
+A step is the whole hot path over one batch: pa_cache_append of the step's
+new token for every sequence, then the paged read (pa_decode).  The
+workload is the Llama-3.2-1B-shaped decode batch: 64 sequences at history
+4096, 32 query / 8 kv heads, head_dim 64, 16-token pages from a 20,000-page
+pool, bf16.  The metric is achieved HBM bandwidth of the step (algorithmic
+bytes / device time, GB/s) with the time per step.
+
+Also reported on the same JSON line: the history sweep {16 .. 4096} of the
+read alone (L2 flushed between launches), the long-context split-KV read +
+merge at 32K and 128K tokens, the ragged 256-sequence batch, the roofline
+of the read kernel, clocks sampled during the run, an end-to-end number
+through the C ABI with host buffers, and the fp64 oracle timed on the host
+cores as a CPU baseline.
+
+``--impl reference`` times the fp64 CPU oracle instead (the slow program
+the pages call the correctness oracle), on host cores, in the same units.
+
+Run: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention: achieved HBM GB/s (% of GB300 peak), µs/step at B=64"
+UNIT = "GB/s"
+L2_BYTES = 129 * 2**20
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_llama1b_h4096.md")
+DOMINANT_SOURCES = ("paged_kv_cache_184_gb300/csrc/pa_decode_simt.cu",
+                    "paged_kv_cache_184_gb300/csrc/pa_common.cuh")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--history", type=int, default=4096)
+    ap.add_argument("--no-extras", action="store_true",
+                    help="headline step only (no sweep, long-context, ragged, CPU baseline)")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------- byte counts
+
+
+def read_bytes(lens, hq, hkv, d, elem, block_size):
+    """Algorithmic bytes of one paged read: K+V rows, q, out, table entries, lengths."""
+    kv = sum(lens) * hkv * d * 2 * elem
+    qo = 2 * len(lens) * hq * d * elem
+    table = 4 * sum(-(-n // block_size) for n in lens) + 4 * len(lens)
+    return kv + qo + table
+
+
+def append_bytes(b, hkv, d, elem):
+    """Read k_new/v_new, write them into the pool, read position, table entry."""
+    return 2 * 2 * b * hkv * d * elem + 8 * b
+
+
+def split_bytes(b, hq, s, d):
+    """Partials written by the split read and read back by the merge."""
+    return 2 * b * hq * s * (d + 1) * 4
+
+
+# ----------------------------------------------------------------- environment
+
+
+def measured_peaks():
+    """HBM copy bandwidth (GB/s) measured on this machine's GPUs, else the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+    except (OSError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+    def find(obj):
+        if isinstance(obj, dict):
+            for k, v in obj.items():
+                if "hbm" in k.lower() and isinstance(v, (int, float)) and v > 100:
+                    return float(v)
+            for v in obj.values():
+                r = find(v)
+                if r is not None:
+                    return r
+        return None
+
+    v = find(j)
+    return (v, "measured") if v is not None else (FALLBACK_HBM_GBS, "fallback")
+
+
+def source_sha():
+    h = hashlib.sha256()
+    for rel in DOMINANT_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it still
+    describes the current kernel source; else None."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    m_sha = re.search(r"source_sha:\s*([0-9a-f]+)", text)
+    m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_sha or not m_tr or m_sha.group(1) != source_sha():
+        return None
+    return float(m_tr.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.dev), "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.3)
+        self.proc.terminate()
+        self.proc.wait(timeout=10)
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) == 9 and parts[1].replace(".", "").isdigit():
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]),
+                "sm_min_mhz": min(sm), "power_w_median": statistics.median(
+                    [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()] or [0.0]),
+                "samples": len(rows), "reasons": reasons}
+
+
+# ----------------------------------------------------------------- CPU oracle timing
+
+
+class OracleSample:
+    """Host copies of a batch for timing the fp64 oracle on whole sequences."""
+
+    def __init__(self, batch_cpu):
+        self.b = batch_cpu
+        self.q = batch_cpu.q.float().numpy()
+        self.kp = batch_cpu.k_pool.float().numpy()
+        self.vp = batch_cpu.v_pool.float().numpy()
+        self.bt = batch_cpu.block_table.numpy()
+        self.lens = batch_cpu.lens_list()
+
+    def run(self, budget_s: float, max_seqs: int, first: int = 0):
+        """Oracle over sequences first, first+1, ... until the budget is spent.
+        Returns (seconds, algorithmic bytes read, sequences done)."""
+        import oracle
+        b = self.b
+        t0 = time.perf_counter()
+        done, nbytes = 0, 0
+        while done < max_seqs:
+            i = (first + done) % len(self.lens)
+            oracle.paged_decode_one(self.q[i], self.kp, self.vp, self.bt[i], self.lens[i],
+                                    b.scale, b.block_size)
+            nbytes += read_bytes([self.lens[i]], b.num_q_heads, b.num_kv_heads, b.head_dim,
+                                 b.q.element_size(), b.block_size)
+            done += 1
+            if time.perf_counter() - t0 > budget_s:
+                break
+        return time.perf_counter() - t0, nbytes, done
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the fp64 oracle on host cores, same workload/metric."""
+    if rank != 0:
+        return
+    import workloads
+    sample = OracleSample(workloads.llama1b(args.history))
+    for k in range(args.warmup):
+        sample.run(0.0, 1, first=k)
+    times, nbytes = [], 0
+    for k in range(args.steps):
+        t, nb, _ = sample.run(0.0, 1, first=k)
+        times.append(t)
+        nbytes += nb
+    total = sum(times)
+    value = nbytes / total / 1e9
+    cores = 1
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(args, world),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"each step: the fp64 oracle over 1 of the 64 sequences "
+                                   f"(history {args.history}, all 32 query heads)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(args, world):
+    return {"workload": f"llama1b decode step: batch 64 per GPU, history {args.history}, "
+                        f"Hq 32 / Hkv 8, head_dim 64, block_size 16, 20,000-page pool, bf16",
+            "global_batch": 64 * world, "seq_len": args.history,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": "inputs larger than L2 (K/V of one step 537 MB vs 129 MB L2)"
+                  if args.history >= 1024 else "L2 flushed between steps"}
+
+
+# ----------------------------------------------------------------- GPU side
+
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("gloo")
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    import paged_kv_cache_184_gb300 as pa
+    import workloads
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    pa.load()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x: float) -> float:
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    # ------------------------------------------------ headline workload
+    cpu = workloads.llama1b(args.history)
+    g = cpu.to(dev)
+    out = torch.empty_like(g.q)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    lens = g.lens_list()
+    elem = g.q.element_size()
+    rb = read_bytes(lens, g.num_q_heads, g.num_kv_heads, g.head_dim, elem, g.block_size)
+    ab = append_bytes(g.num_seqs, g.num_kv_heads, g.head_dim, elem)
+    step_bytes = rb + ab
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    small = args.history < 1024  # history too short to exceed L2 by itself
+
+    def step():
+        pa.pa_cache_append(g.k_new, g.v_new, g.k_pool, g.v_pool, g.block_table, g.positions,
+                           dev_err=err)
+        pa.pa_decode(out, g.q, g.k_pool, g.v_pool, g.block_table, g.seq_lens, g.scale,
+                     dev_err=err)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    t_end = time.perf_counter() + 1.0        # keep the GPU loaded so clocks settle
+    while time.perf_counter() < t_end:
+        for _ in range(50):
+            step()
+        torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    for k in range(args.steps):
+        if small:
+            flush.zero_()
+        ev[k][0].record(stream)
+        pa.pa_cache_append(g.k_new, g.v_new, g.k_pool, g.v_pool, g.block_table, g.positions,
+                           dev_err=err)
+        ev[k][1].record(stream)
+        pa.pa_decode(out, g.q, g.k_pool, g.v_pool, g.block_table, g.seq_lens, g.scale,
+                     dev_err=err)
+        ev[k][2].record(stream)
+    barrier()
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(c) for a, _, c in ev]
+    dec_ms = [b.elapsed_time(c) for _, b, c in ev]
+    ms_per_step = max_over_ranks(sum(step_ms) / args.steps)
+    dec_avg_ms = sum(dec_ms) / args.steps
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error {int(err.item())} during the timed steps")
+    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    achieved = rb / (dec_avg_ms * 1e-3) / 1e9
+    gpu_launches = 2 * args.steps
+
+    # ------------------------------------------------ end to end with host buffers
+    pin = lambda t: t.cpu().pin_memory()
+    h_in = {n: pin(getattr(cpu, n)) for n in ("q", "k_new", "v_new", "positions", "seq_lens",
+                                              "block_table")}
+    h_out = torch.empty(cpu.q.shape, dtype=cpu.q.dtype).pin_memory()
+    d_in = {n: getattr(g, n) for n in h_in}
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        for n, t in h_in.items():
+            d_in[n].copy_(t, non_blocking=True)
+        pa.pa_cache_append(d_in["k_new"], d_in["v_new"], g.k_pool, g.v_pool, d_in["block_table"],
+                           d_in["positions"], dev_err=err)
+        pa.pa_decode(out, d_in["q"], g.k_pool, g.v_pool, d_in["block_table"], d_in["seq_lens"],
+                     g.scale, dev_err=err)
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        if small:
+            flush.zero_()
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
+    e2e_value = world * step_bytes / (e2e_ms * 1e-3) / 1e9
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "us_per_step": 1e3 * ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded N(0,1) bf16 q/K/V, random non-contiguous block tables",
+        "config": workload_config(args, world),
+        "clocks": clk,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": gpu_launches,
+        "roofline": {"bound": "hbm", "kernel": "pa_decode (decode_simt_kernel)",
+                     "achieved": achieved, "peak": peak, "peak_source": peak_kind,
+                     "unit": "GB/s", "frac": achieved / peak,
+                     "frac_of_nominal_8tbs": achieved / 8000.0,
+                     "traffic": profiled_traffic(), "algorithmic_bytes_per_launch": rb,
+                     "us_per_launch": 1e3 * dec_avg_ms},
+        "bytes_per_step": step_bytes,
+    }
+
+    if rank == 0 and not args.no_extras:
+        line["sweep"] = sweep(pa, workloads, torch, dev, flush, peak)
+        line["longctx"] = longctx(pa, workloads, torch, dev, peak)
+        line["ragged8b"] = ragged(pa, workloads, torch, dev, peak)
+        if world == 1:
+            t, nb, n = OracleSample(cpu).run(12.0, 64)
+            line["cpu_baseline"] = {
+                "value": nb / t / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+                "sample": f"{n} whole sequences of the headline batch (history {args.history}, "
+                          f"32 query heads each), fp64 NumPy, one thread"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def _time_launches(fn, torch, flush, iters=30, warm=3):
+    """Median / min device time (ms) of fn over iters launches, L2 flushed before each."""
+    stream = torch.cuda.current_stream()
+    for _ in range(warm):
+        fn()
+    ts = []
+    for _ in range(iters):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in ts]
+    return statistics.median(ms), min(ms)
+
+
+def sweep(pa, workloads, torch, dev, flush, peak):
+    rows = []
+    for h in workloads.LLAMA1B_HISTORIES:
+        g = workloads.llama1b(h, device=str(dev))
+        out = torch.empty_like(g.q)
+        fn = lambda: pa.pa_decode(out, g.q, g.k_pool, g.v_pool, g.block_table, g.seq_lens, g.scale)
+        med, mn = _time_launches(fn, torch, flush)
+        rb = read_bytes(g.lens_list(), 32, 8, 64, 2, 16)
+        rows.append({"history": h, "us_median": 1e3 * med, "us_min": 1e3 * mn,
+                     "gbs": rb / (med * 1e-3) / 1e9, "frac": rb / (med * 1e-3) / 1e9 / peak})
+        del g, out
+    torch.cuda.empty_cache()
+    return rows
+
+
+def longctx(pa, workloads, torch, dev, peak):
+    rows = []
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    for h in workloads.LONGCTX_HISTORIES:
+        g = workloads.longctx(h, device=str(dev))
+        s = pa.pa_num_splits(g.max_blocks, g.pages_per_split)
+        po = torch.empty((g.num_seqs, g.num_q_heads, s, g.head_dim), device=dev)
+        pl = torch.empty((g.num_seqs, g.num_q_heads, s), device=dev)
+        out = torch.empty_like(g.q)
+
+        def fn():
+            pa.pa_decode_splitkv(po, pl, g.q, g.k_pool, g.v_pool, g.block_table, g.seq_lens,
+                                 g.scale, g.pages_per_split)
+            pa.pa_merge(out, po, pl)
+
+        med, mn = _time_launches(fn, torch, flush, iters=20)
+        rb = read_bytes(g.lens_list(), 32, 8, 128, 2, 16) + split_bytes(g.num_seqs, 32, s, 128)
+        single = lambda: pa.pa_decode(out, g.q, g.k_pool, g.v_pool, g.block_table, g.seq_lens,
+                                      g.scale)
+        med1, _ = _time_launches(single, torch, flush, iters=10)
+        rows.append({"history": h, "splits": s, "us_split_plus_merge": 1e3 * med,
+                     "gbs": rb / (med * 1e-3) / 1e9, "frac": rb / (med * 1e-3) / 1e9 / peak,
+                     "us_single_pass": 1e3 * med1})
+        del g, po, pl, out
+        torch.cuda.empty_cache()
+    return rows
+
+
+def ragged(pa, workloads, torch, dev, peak):
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    g = workloads.ragged8b(device=str(dev))
+    out = torch.empty_like(g.q)
+    s = pa.pa_num_splits(g.max_blocks, 64)
+    po = torch.empty((g.num_seqs, g.num_q_heads, s, g.head_dim), device=dev)
+    pl = torch.empty((g.num_seqs, g.num_q_heads, s), device=dev)
+    single = lambda: pa.pa_decode(out, g.q, g.k_pool, g.v_pool, g.block_table, g.seq_lens, g.scale)
+
+    def split():
+        pa.pa_decode_splitkv(po, pl, g.q, g.k_pool, g.v_pool, g.block_table, g.seq_lens, g.scale, 64)
+        pa.pa_merge(out, po, pl)
+
+    med1, _ = _time_launches(single, torch, flush, iters=10)
+    med2, _ = _time_launches(split, torch, flush, iters=10)
+    rb = read_bytes(g.lens_list(), 32, 8, 128, 2, 16)
+    res = {"batch": g.num_seqs, "kv_gb": g.kv_bytes() / 1e9,
+           "us_single_pass": 1e3 * med1, "gbs_single_pass": rb / (med1 * 1e-3) / 1e9,
+           "us_split64_plus_merge": 1e3 * med2,
+           "gbs_split64": (rb + split_bytes(g.num_seqs, 32, s, 128)) / (med2 * 1e-3) / 1e9}
+    res["frac_best"] = max(res["gbs_single_pass"], res["gbs_split64"]) / peak
+    del g, out, po, pl
+    torch.cuda.empty_cache()
+    return res
+
+
+if __name__ == "__main__":
+    main()

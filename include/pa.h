@@ -1,0 +1,177 @@
+/*
+ * pa.h - C ABI of the GB300 paged KV-cache decode-attention library (libpa.so).
+ *
+ * The cache is a fixed pool of pages.  A page holds block_size consecutive
+ * tokens of one sequence; a sequence's block table lists its pages in order,
+ * so token p of sequence b lives at slot p % block_size of page
+ * block_table[b][p / block_size] ("triton-attention-kernels", section
+ * "3. Paged KV-cache attention": the page comes from the block table, the
+ * row from the offset inside the page).
+ *
+ * Memory layouts (row-major, contiguous, no padding):
+ *   q, out        [num_seqs][num_q_heads][head_dim]                      dtype
+ *   k_pool,v_pool [num_pages][block_size][num_kv_heads][head_dim]        dtype
+ *   k_new,v_new   [num_tokens][num_kv_heads][head_dim]                   dtype
+ *   block_table   [num_seqs][max_blocks_per_seq]                         int32
+ *   seq_lens      [num_seqs]                                             int32
+ *   partial_out   [num_seqs][num_q_heads][max_splits][head_dim]          float
+ *   partial_lse   [num_seqs][num_q_heads][max_splits]                    float
+ * Query head h reads kv head h / (num_q_heads / num_kv_heads) (grouped-query
+ * attention with contiguous groups).
+ *
+ * Ownership: every pointer is device memory owned by the caller.  The
+ * library allocates no memory, keeps no state between calls, and launches
+ * its kernels asynchronously on the caller's stream; the call returns once
+ * the launch is queued.
+ *
+ * Errors: argument checks run on the host before any launch and return
+ * PA_ERR_INVALID_ARG (a null or misaligned pointer, a negative or
+ * inconsistent size) or PA_ERR_UNSUPPORTED (a valid shape the kernels do
+ * not cover); nothing is launched then.  PA_ERR_CUDA means the launch
+ * itself failed.  Values that live on the device (block-table entries,
+ * sequence lengths, positions, sequence ids) are checked by the kernels:
+ * an out-of-range value makes the kernel skip the memory access, write
+ * zeros to the outputs it owns (lse -inf for split partials) and record the
+ * first such error code in *dev_err (atomic compare-and-swap from 0; a null
+ * dev_err only skips the recording).  No kernel traps or waits on another.
+ *
+ * Supported: dtype f32, f16 or bf16, the same for q, the pools, k_new/v_new
+ * and out; head_dim * element size a multiple of 16 bytes and head_dim at
+ * most 256; num_q_heads a multiple of num_kv_heads with at most 8 query
+ * heads per kv head; block_size a power of two from 1 to 1024; num_seqs at
+ * most 65535.  All data pointers 16-byte aligned.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL selects the legacy default stream. */
+typedef struct CUstream_st *pa_stream_t;
+
+typedef enum pa_status {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1,
+  PA_ERR_UNSUPPORTED = 2,
+  PA_ERR_CUDA = 3
+} pa_status;
+
+typedef enum pa_dtype { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2 } pa_dtype;
+
+/* Codes a kernel records in *dev_err. */
+enum {
+  PA_DEV_OK = 0,
+  PA_DEV_BAD_PAGE = 1,     /* block-table entry outside [0, num_pages) */
+  PA_DEV_BAD_POSITION = 2, /* append position outside [0, max_blocks_per_seq * block_size) */
+  PA_DEV_BAD_SEQ_LEN = 3,  /* seq_len outside [0, max_blocks_per_seq * block_size] */
+  PA_DEV_BAD_SEQ_ID = 4    /* append seq id outside [0, num_seqs) */
+};
+
+/* Human-readable name of a status code (static string). */
+const char *pa_status_string(pa_status status);
+
+/* Library version string (static). */
+const char *pa_version(void);
+
+/* Splits per sequence for a split-KV read: ceil(max_blocks_per_seq /
+ * pages_per_split), or 0 if either argument is not positive.  Sizes
+ * partial_out and partial_lse. */
+int32_t pa_num_splits(int32_t max_blocks_per_seq, int32_t pages_per_split);
+
+/*
+ * pa_cache_append - write new tokens' K and V into their page slots.
+ *
+ * nanoserve "Day 20: the number the Triton kernel has to beat", section
+ * "What I learned": the cache write grows the block table and scatters the
+ * K/V.  The table is grown by the caller (page allocation is host-side);
+ * this call is the scatter.  Token i belongs to sequence seq_ids[i] (token
+ * i belongs to sequence i when seq_ids is NULL) and is stored at position
+ * positions[i]: k_new[i] (num_kv_heads * head_dim elements) is copied to
+ * k_pool[block_table[seq][pos / block_size]][pos % block_size], likewise V.
+ * A pure byte copy (no conversion): bit-exact, every other pool byte keeps
+ * its value.  Two tokens of one call that name the same slot race.
+ * num_tokens == 0 is a no-op.  num_seqs is the number of block-table rows.
+ */
+pa_status pa_cache_append(const void *k_new, const void *v_new, void *k_pool,
+                          void *v_pool, const int32_t *block_table,
+                          int32_t num_seqs, int32_t max_blocks_per_seq,
+                          const int32_t *seq_ids, const int32_t *positions,
+                          int32_t num_tokens, int32_t num_pages,
+                          int32_t num_kv_heads, int32_t head_dim,
+                          int32_t block_size, pa_dtype dtype, int32_t *dev_err,
+                          pa_stream_t stream);
+
+/*
+ * pa_decode - one decode step of attention over the paged cache.
+ *
+ * For every sequence b and query head h (kv head g = h / group):
+ *   out[b][h] = softmax_t(scale * q[b][h] . K_b[t][g]) @ V_b[t][g],
+ *   t = 0 .. seq_lens[b]-1,
+ * where K_b[t] is read through the block table.  This is attention
+ * softmax(Q K^T / sqrt(d)) V ("triton-attention-kernels", section "What is
+ * attention, really?") at decode (one query per sequence), computed in one
+ * streaming pass with an online softmax (a running max and sum, the score
+ * row never stored) as nanoserve "Day 23: the real triton.jit
+ * paged-attention kernel" streams its tiles.  seq_lens[b] counts every
+ * attended token, including one appended this step.  A length of 0 gives
+ * out = 0.  Accumulation is in fp32; out is rounded to dtype
+ * (round-to-nearest-even).
+ */
+pa_status pa_decode(void *out, const void *q, const void *k_pool,
+                    const void *v_pool, const int32_t *block_table,
+                    int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                    int32_t num_seqs, int32_t num_q_heads,
+                    int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                    int32_t num_pages, float scale, pa_dtype dtype,
+                    int32_t *dev_err, pa_stream_t stream);
+
+/*
+ * pa_decode_splitkv - the same read, split along the history.
+ *
+ * "triton-attention-kernels", section "2. Split-KV flash-decoding": each
+ * split reduces its own slice of K/V to a partial output and a log-sum-exp,
+ * and a final cross-split combine (pa_merge) gives the output.  Here a split
+ * is a fixed run of pages_per_split pages: split s of sequence b covers
+ * tokens [s * pages_per_split * block_size, min(seq_lens[b], (s+1) *
+ * pages_per_split * block_size)).  For every split it writes
+ *   partial_out[b][h][s] = softmax-weighted V over the split (fp32),
+ *   partial_lse[b][h][s] = log(sum_t exp(scale * q . k_t)) over the split,
+ * and for a split with no tokens partial_out = 0, partial_lse = -inf.
+ * max_splits must be at least pa_num_splits(max_blocks_per_seq,
+ * pages_per_split); it is the split stride of the partial arrays.
+ */
+pa_status pa_decode_splitkv(float *partial_out, float *partial_lse,
+                            const void *q, const void *k_pool,
+                            const void *v_pool, const int32_t *block_table,
+                            int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                            int32_t num_seqs, int32_t num_q_heads,
+                            int32_t num_kv_heads, int32_t head_dim,
+                            int32_t block_size, int32_t num_pages, float scale,
+                            int32_t pages_per_split, int32_t max_splits,
+                            pa_dtype dtype, int32_t *dev_err,
+                            pa_stream_t stream);
+
+/*
+ * pa_merge - combine split partials into the output.
+ *
+ * "triton-attention-kernels", section "2. Split-KV flash-decoding", the
+ * cross-SM combine: for every (b, h), M = max_s partial_lse[b][h][s],
+ * w_s = exp(partial_lse[b][h][s] - M), and
+ *   out[b][h] = sum_s w_s * partial_out[b][h][s] / sum_s w_s,
+ * rounded to dtype.  A row whose splits are all empty (every lse -inf)
+ * gives 0.  fp32 arithmetic.
+ */
+pa_status pa_merge(void *out, const float *partial_out,
+                   const float *partial_lse, int32_t num_seqs,
+                   int32_t num_q_heads, int32_t max_splits, int32_t head_dim,
+                   pa_dtype dtype, pa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

@@ -1,0 +1,198 @@
+"""Python binding of libpa.so, the GB300 paged KV-cache decode-attention library.
+
+Argument marshalling only: every function here takes torch tensors, checks
+that they are contiguous device tensors, reads their shapes, and passes raw
+pointers and sizes to the C ABI declared in include/pa.h, on the current
+CUDA stream.  All arithmetic runs in the library's CUDA kernels; there is
+no other implementation to fall back on, so a missing library raises.
+
+The names match the C ABI: pa_cache_append, pa_decode, pa_decode_splitkv,
+pa_merge, pa_num_splits, pa_status_string, pa_version.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+from . import _build
+
+LIB_PATH = _build.LIB_PATH
+
+PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA = 0, 1, 2, 3
+PA_F32, PA_F16, PA_BF16 = 0, 1, 2
+PA_DEV_OK, PA_DEV_BAD_PAGE, PA_DEV_BAD_POSITION, PA_DEV_BAD_SEQ_LEN, PA_DEV_BAD_SEQ_ID = 0, 1, 2, 3, 4
+
+EXPORTED = ("pa_status_string", "pa_version", "pa_num_splits", "pa_cache_append",
+            "pa_decode", "pa_decode_splitkv", "pa_merge")
+
+_lib: Optional[ctypes.CDLL] = None
+
+_p = ctypes.c_void_p
+_i = ctypes.c_int32
+_f = ctypes.c_float
+
+_SIGNATURES = {
+    "pa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "pa_version": (ctypes.c_char_p, []),
+    "pa_num_splits": (_i, [_i, _i]),
+    "pa_cache_append": (ctypes.c_int, [_p, _p, _p, _p, _p, _i, _i, _p, _p, _i, _i, _i, _i, _i,
+                                       ctypes.c_int, _p, _p]),
+    "pa_decode": (ctypes.c_int, [_p, _p, _p, _p, _p, _i, _p, _i, _i, _i, _i, _i, _i, _f,
+                                 ctypes.c_int, _p, _p]),
+    "pa_decode_splitkv": (ctypes.c_int, [_p, _p, _p, _p, _p, _p, _i, _p, _i, _i, _i, _i, _i, _i,
+                                         _f, _i, _i, ctypes.c_int, _p, _p]),
+    "pa_merge": (ctypes.c_int, [_p, _p, _p, _i, _i, _i, _i, ctypes.c_int, _p]),
+}
+
+
+class PaError(RuntimeError):
+    """A C-ABI call returned a status other than PA_OK."""
+
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} returned {status} ({pa_status_string(status)})")
+
+
+def load(build: bool = True) -> ctypes.CDLL:
+    """Load libpa.so (building it first when asked and out of date)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if build:
+        _build.build()
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"libpa.so not built at {LIB_PATH}; run paged_kv_cache_184_gb300._build")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def raw() -> ctypes.CDLL:
+    """The loaded ctypes library, for callers that pass raw pointers."""
+    return load()
+
+
+def _dtype_code(t) -> int:
+    import torch
+    codes = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16}
+    if t.dtype not in codes:
+        raise ValueError(f"unsupported dtype {t.dtype}")
+    return codes[t.dtype]
+
+
+def _ptr(t, name: str, dtype=None, allow_none: bool = False):
+    if t is None:
+        if allow_none:
+            return None
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(fn: str, status: int) -> None:
+    if status != PA_OK:
+        raise PaError(fn, status)
+
+
+def pa_status_string(status: int) -> str:
+    return load().pa_status_string(status).decode()
+
+
+def pa_version() -> str:
+    return load().pa_version().decode()
+
+
+def pa_num_splits(max_blocks_per_seq: int, pages_per_split: int) -> int:
+    return int(load().pa_num_splits(max_blocks_per_seq, pages_per_split))
+
+
+def pa_cache_append(k_new, v_new, k_pool, v_pool, block_table, positions, seq_ids=None,
+                    dev_err=None, stream=None) -> None:
+    """Scatter k_new/v_new [T, Hkv, d] into their page slots of k_pool/v_pool."""
+    import torch
+    lib = load()
+    num_pages, block_size, hkv, d = k_pool.shape
+    if v_pool.shape != k_pool.shape or k_new.shape != v_new.shape or k_new.shape[1:] != (hkv, d):
+        raise ValueError("pa_cache_append: inconsistent K/V shapes")
+    dt = k_pool.dtype
+    st = lib.pa_cache_append(
+        _ptr(k_new, "k_new", dt), _ptr(v_new, "v_new", dt), _ptr(k_pool, "k_pool", dt),
+        _ptr(v_pool, "v_pool", dt), _ptr(block_table, "block_table", torch.int32),
+        block_table.shape[0], block_table.shape[1],
+        _ptr(seq_ids, "seq_ids", torch.int32, allow_none=True),
+        _ptr(positions, "positions", torch.int32), k_new.shape[0], num_pages, hkv, d,
+        block_size, _dtype_code(k_pool), _ptr(dev_err, "dev_err", torch.int32, allow_none=True),
+        _stream(stream))
+    _check("pa_cache_append", st)
+
+
+def pa_decode(out, q, k_pool, v_pool, block_table, seq_lens, scale: float, dev_err=None,
+              stream=None) -> None:
+    """out[b, h] = softmax(scale * q[b, h] . K_b) V_b over the paged history."""
+    import torch
+    lib = load()
+    num_pages, block_size, hkv, d = k_pool.shape
+    b, hq, dq = q.shape
+    if dq != d or out.shape != q.shape or v_pool.shape != k_pool.shape:
+        raise ValueError("pa_decode: inconsistent shapes")
+    dt = q.dtype
+    st = lib.pa_decode(
+        _ptr(out, "out", dt), _ptr(q, "q", dt), _ptr(k_pool, "k_pool", dt),
+        _ptr(v_pool, "v_pool", dt), _ptr(block_table, "block_table", torch.int32),
+        block_table.shape[1], _ptr(seq_lens, "seq_lens", torch.int32), b, hq, hkv, d,
+        block_size, num_pages, float(scale), _dtype_code(q),
+        _ptr(dev_err, "dev_err", torch.int32, allow_none=True), _stream(stream))
+    _check("pa_decode", st)
+
+
+def pa_decode_splitkv(partial_out, partial_lse, q, k_pool, v_pool, block_table, seq_lens,
+                      scale: float, pages_per_split: int, dev_err=None, stream=None) -> None:
+    """Per-split partial outputs [B, Hq, S, d] and lse [B, Hq, S] (float32)."""
+    import torch
+    lib = load()
+    num_pages, block_size, hkv, d = k_pool.shape
+    b, hq, _ = q.shape
+    max_splits = partial_lse.shape[2]
+    if partial_out.shape != (b, hq, max_splits, d) or partial_lse.shape != (b, hq, max_splits):
+        raise ValueError("pa_decode_splitkv: partial shapes must be [B,Hq,S,d] and [B,Hq,S]")
+    dt = q.dtype
+    st = lib.pa_decode_splitkv(
+        _ptr(partial_out, "partial_out", torch.float32),
+        _ptr(partial_lse, "partial_lse", torch.float32), _ptr(q, "q", dt),
+        _ptr(k_pool, "k_pool", dt), _ptr(v_pool, "v_pool", dt),
+        _ptr(block_table, "block_table", torch.int32), block_table.shape[1],
+        _ptr(seq_lens, "seq_lens", torch.int32), b, hq, hkv, d, block_size, num_pages,
+        float(scale), int(pages_per_split), max_splits, _dtype_code(q),
+        _ptr(dev_err, "dev_err", torch.int32, allow_none=True), _stream(stream))
+    _check("pa_decode_splitkv", st)
+
+
+def pa_merge(out, partial_out, partial_lse, stream=None) -> None:
+    """out[b, h] = sum_s w_s partial_out[b, h, s] / sum_s w_s, w_s = exp(lse_s - max lse)."""
+    import torch
+    lib = load()
+    b, hq, s, d = partial_out.shape
+    if out.shape != (b, hq, d) or partial_lse.shape != (b, hq, s):
+        raise ValueError("pa_merge: inconsistent shapes")
+    st = lib.pa_merge(_ptr(out, "out"), _ptr(partial_out, "partial_out", torch.float32),
+                      _ptr(partial_lse, "partial_lse", torch.float32), b, hq, s, d,
+                      _dtype_code(out), _stream(stream))
+    _check("pa_merge", st)

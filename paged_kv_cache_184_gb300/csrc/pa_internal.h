@@ -1,0 +1,51 @@
+// Internal interface between the C-ABI layer (pa_api.cu) and the kernels.
+// Every pointer is caller-owned device memory; every size was validated by
+// the C-ABI layer before any launcher here is called.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pa.h"
+
+namespace pa {
+
+// Arguments of one paged read (pa_decode or pa_decode_splitkv).
+struct DecodeParams {
+  void *out;            // [B][Hq][D] dtype; unused by the split-KV read
+  float *partial_out;   // [B][Hq][max_splits][D]; split-KV read only
+  float *partial_lse;   // [B][Hq][max_splits];    split-KV read only
+  const void *q;        // [B][Hq][D]
+  const void *k_pool;   // [num_pages][block_size][Hkv][D]
+  const void *v_pool;
+  const int32_t *block_table;  // [B][max_blocks]
+  const int32_t *seq_lens;     // [B]
+  int32_t *dev_err;            // nullable
+  int32_t num_seqs, num_q_heads, num_kv_heads, head_dim, group;
+  int32_t max_blocks, block_size_log2, num_pages;
+  int32_t pages_per_split;  // 0: one split spanning the whole sequence
+  int32_t num_splits;       // grid splits per sequence (1 when pages_per_split == 0)
+  float scale_log2;         // scale * log2(e): scores kept in base-2 units
+};
+
+struct AppendParams {
+  const void *k_new, *v_new;  // [T][Hkv][D]
+  void *k_pool, *v_pool;
+  const int32_t *block_table, *seq_ids, *positions;
+  int32_t *dev_err;
+  int32_t num_seqs, max_blocks, num_tokens, num_pages, block_size_log2;
+  int32_t row_chunks;  // 16-byte chunks in one token row (Hkv * D * elem / 16)
+};
+
+struct MergeParams {
+  void *out;
+  const float *partial_out, *partial_lse;
+  int32_t rows;  // B * Hq
+  int32_t num_splits, head_dim;
+};
+
+cudaError_t launch_decode_simt(const DecodeParams &p, pa_dtype dtype, cudaStream_t stream);
+cudaError_t launch_append(const AppendParams &p, cudaStream_t stream);
+cudaError_t launch_merge(const MergeParams &p, pa_dtype dtype, cudaStream_t stream);
+
+}  // namespace pa

@@ -1,0 +1,160 @@
+"""Host-side checks of the C ABI: the library loads, exports what include/pa.h
+declares, and rejects bad arguments before launching anything.
+
+No call here reaches a kernel launch: every call is either a pure host
+function or one that the validation layer must refuse (or treat as an empty
+no-op) before any CUDA call.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_cache_184_gb300 as pa
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "pa.h")
+
+# non-null, 16-byte aligned stand-ins that are never dereferenced
+FAKE = 0x10000
+MISALIGNED = 0x10008
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_library_builds_and_exports_every_declared_symbol(lib):
+    raw = lib.raw()
+    names = declared_functions()
+    assert set(names) == set(pa.EXPORTED)
+    for n in names:
+        assert hasattr(raw, n), n
+
+
+def test_status_strings_and_version(lib):
+    assert lib.pa_status_string(0) == "PA_OK"
+    assert lib.pa_status_string(1) == "PA_ERR_INVALID_ARG"
+    assert lib.pa_status_string(2) == "PA_ERR_UNSUPPORTED"
+    assert lib.pa_status_string(3) == "PA_ERR_CUDA"
+    assert lib.pa_status_string(99) == "PA_ERR_UNKNOWN"
+    assert "sm_103a" in lib.pa_version()
+
+
+@pytest.mark.parametrize("mb,pps,want", [(256, 64, 4), (257, 64, 5), (1, 64, 1), (64, 1, 64),
+                                          (8192, 64, 128), (0, 64, 0), (5, 0, 0), (-1, 4, 0)])
+def test_num_splits(lib, mb, pps, want):
+    assert lib.pa_num_splits(mb, pps) == want
+
+
+def _decode(raw, **kw):
+    a = dict(out=FAKE, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, mb=4, sl=FAKE, b=2, hq=8, hkv=2, d=64,
+             bs=16, np_=32, scale=0.125, dt=pa.PA_BF16)
+    a.update(kw)
+    return raw.pa_decode(a["out"], a["q"], a["k"], a["v"], a["bt"], a["mb"], a["sl"], a["b"],
+                         a["hq"], a["hkv"], a["d"], a["bs"], a["np_"], a["scale"], a["dt"],
+                         None, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(hq=9, hkv=2), pa.PA_ERR_INVALID_ARG),          # group not integral
+    (dict(hkv=0), pa.PA_ERR_INVALID_ARG),
+    (dict(d=0), pa.PA_ERR_INVALID_ARG),
+    (dict(d=36), pa.PA_ERR_UNSUPPORTED),                 # 72 bytes: not a multiple of 16
+    (dict(d=512), pa.PA_ERR_UNSUPPORTED),                # beyond 256
+    (dict(d=6, dt=pa.PA_F32), pa.PA_ERR_UNSUPPORTED),    # 24 bytes
+    (dict(hq=18, hkv=1), pa.PA_ERR_UNSUPPORTED),         # group of 18
+    (dict(bs=12), pa.PA_ERR_INVALID_ARG),                # not a power of two
+    (dict(bs=0), pa.PA_ERR_INVALID_ARG),
+    (dict(bs=2048), pa.PA_ERR_UNSUPPORTED),
+    (dict(mb=0), pa.PA_ERR_INVALID_ARG),
+    (dict(np_=0), pa.PA_ERR_INVALID_ARG),
+    (dict(b=-1), pa.PA_ERR_INVALID_ARG),
+    (dict(b=70000), pa.PA_ERR_UNSUPPORTED),
+    (dict(dt=7), pa.PA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), pa.PA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), pa.PA_ERR_INVALID_ARG),
+    (dict(q=None), pa.PA_ERR_INVALID_ARG),
+    (dict(sl=None), pa.PA_ERR_INVALID_ARG),
+    (dict(k=MISALIGNED), pa.PA_ERR_INVALID_ARG),
+    (dict(out=MISALIGNED), pa.PA_ERR_INVALID_ARG),
+    (dict(b=0), pa.PA_OK),                               # empty batch: nothing to launch
+])
+def test_decode_validation(lib, kw, want):
+    assert _decode(lib.raw(), **kw) == want
+
+
+def _split(raw, **kw):
+    a = dict(po=FAKE, pl=FAKE, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, mb=10, sl=FAKE, b=2, hq=8, hkv=2,
+             d=64, bs=16, np_=32, scale=0.125, pps=4, ms=3, dt=pa.PA_F16)
+    a.update(kw)
+    return raw.pa_decode_splitkv(a["po"], a["pl"], a["q"], a["k"], a["v"], a["bt"], a["mb"],
+                                 a["sl"], a["b"], a["hq"], a["hkv"], a["d"], a["bs"], a["np_"],
+                                 a["scale"], a["pps"], a["ms"], a["dt"], None, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(ms=2), pa.PA_ERR_INVALID_ARG),                 # 10 pages / 4 per split needs 3
+    (dict(pps=0), pa.PA_ERR_INVALID_ARG),
+    (dict(pl=None), pa.PA_ERR_INVALID_ARG),
+    (dict(po=MISALIGNED), pa.PA_ERR_INVALID_ARG),
+    (dict(hq=6, hkv=4), pa.PA_ERR_INVALID_ARG),
+    (dict(b=0), pa.PA_OK),
+])
+def test_splitkv_validation(lib, kw, want):
+    assert _split(lib.raw(), **kw) == want
+
+
+@pytest.mark.parametrize("args,want", [
+    ((FAKE, FAKE, FAKE, 2, 4, 0, 64, pa.PA_BF16), pa.PA_ERR_INVALID_ARG),   # no splits
+    ((FAKE, FAKE, FAKE, 2, 4, 3, 0, pa.PA_BF16), pa.PA_ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, 2, 4, 3, 320, pa.PA_BF16), pa.PA_ERR_UNSUPPORTED),
+    ((FAKE, FAKE, FAKE, 2, 4, 3, 64, 5), pa.PA_ERR_INVALID_ARG),
+    ((None, FAKE, FAKE, 2, 4, 3, 64, pa.PA_BF16), pa.PA_ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, 0, 4, 3, 64, pa.PA_BF16), pa.PA_OK),
+])
+def test_merge_validation(lib, args, want):
+    assert lib.raw().pa_merge(*args, None) == want
+
+
+def _append(raw, **kw):
+    a = dict(kn=FAKE, vn=FAKE, kp=FAKE, vp=FAKE, bt=FAKE, ns=4, mb=8, sid=None, pos=FAKE, nt=4,
+             np_=32, hkv=8, d=64, bs=16, dt=pa.PA_BF16)
+    a.update(kw)
+    return raw.pa_cache_append(a["kn"], a["vn"], a["kp"], a["vp"], a["bt"], a["ns"], a["mb"],
+                               a["sid"], a["pos"], a["nt"], a["np_"], a["hkv"], a["d"], a["bs"],
+                               a["dt"], None, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(nt=5), pa.PA_ERR_INVALID_ARG),                 # token i -> seq i needs nt <= ns
+    (dict(bs=3), pa.PA_ERR_INVALID_ARG),
+    (dict(bs=4096), pa.PA_ERR_UNSUPPORTED),
+    (dict(hkv=1, d=4), pa.PA_ERR_UNSUPPORTED),           # 8-byte rows
+    (dict(pos=None), pa.PA_ERR_INVALID_ARG),
+    (dict(kp=MISALIGNED), pa.PA_ERR_INVALID_ARG),
+    (dict(nt=-1), pa.PA_ERR_INVALID_ARG),
+    (dict(dt=9), pa.PA_ERR_INVALID_ARG),
+    (dict(nt=0), pa.PA_OK),
+    (dict(nt=0, kn=None), pa.PA_OK),                     # empty append touches nothing
+])
+def test_append_validation(lib, kw, want):
+    assert _append(lib.raw(), **kw) == want
+
+
+def test_binding_rejects_host_tensors(lib):
+    import torch
+    q = torch.zeros(1, 4, 64, dtype=torch.bfloat16)
+    kp = torch.zeros(2, 16, 1, 64, dtype=torch.bfloat16)
+    bt = torch.zeros(1, 2, dtype=torch.int32)
+    sl = torch.ones(1, dtype=torch.int32)
+    with pytest.raises(ValueError):
+        lib.pa_decode(torch.empty_like(q), q, kp, kp, bt, sl, 0.125)
+
+
+def test_binding_raises_on_bad_status(lib):
+    assert isinstance(pa.PaError("pa_decode", 2), RuntimeError)
+    assert "PA_ERR_UNSUPPORTED" in str(pa.PaError("pa_decode", 2))
