@@ -43,7 +43,7 @@ UNIT = "GB/s"
 L2_BYTES = 129 * 2**20
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_llama1b_h4096.md")
-DOMINANT_SOURCES = ("paged_kv_cache_184_gb300/csrc/pa_decode_simt.cu",
+DOMINANT_SOURCES = ("paged_kv_cache_184_gb300/csrc/pa_decode_mma.cu",
                     "paged_kv_cache_184_gb300/csrc/pa_common.cuh")
 
 
@@ -388,7 +388,7 @@ def main():
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": gpu_launches,
-        "roofline": {"bound": "hbm", "kernel": "pa_decode (decode_simt_kernel)",
+        "roofline": {"bound": "hbm", "kernel": "pa_decode (decode_mma_kernel)",
                      "achieved": achieved, "peak": peak, "peak_source": peak_kind,
                      "unit": "GB/s", "frac": achieved / peak,
                      "frac_of_nominal_8tbs": achieved / 8000.0,

@@ -38,7 +38,8 @@
  * Supported: dtype f32, f16 or bf16, the same for q, the pools, k_new/v_new
  * and out; head_dim * element size a multiple of 16 bytes and head_dim at
  * most 256; num_q_heads a multiple of num_kv_heads with at most 8 query
- * heads per kv head; block_size a power of two from 1 to 1024; num_seqs at
+ * heads per kv head (16 for f16/bf16 with head_dim 32, 48, 64, 96, 128 or
+ * 256); block_size a power of two from 1 to 1024; num_seqs at
  * most 65535.  All data pointers 16-byte aligned.
  */
 #ifndef PA_H_

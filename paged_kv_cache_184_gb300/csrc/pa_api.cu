@@ -14,7 +14,8 @@
 namespace {
 
 constexpr int32_t kMaxHeadDim = 256;
-constexpr int32_t kMaxGroup = 8;
+constexpr int32_t kMaxGroupSimt = 8;   // CUDA-core read
+constexpr int32_t kMaxGroupMma = 16;   // tensor-core read
 constexpr int32_t kMaxBlockSize = 1024;
 constexpr int32_t kMaxSeqs = 65535;  // grid.y
 
@@ -49,7 +50,9 @@ pa_status check_read_shape(int32_t max_blocks, int32_t num_seqs, int32_t hq, int
   if (log2_exact(block_size) < 0) return PA_ERR_INVALID_ARG;
   if (block_size > kMaxBlockSize) return PA_ERR_UNSUPPORTED;
   if ((static_cast<int64_t>(d) * es) % 16 != 0 || d > kMaxHeadDim) return PA_ERR_UNSUPPORTED;
-  if (hq / hkv > kMaxGroup) return PA_ERR_UNSUPPORTED;
+  const int group = hq / hkv;
+  if (group > kMaxGroupMma) return PA_ERR_UNSUPPORTED;
+  if (group > kMaxGroupSimt && !pa::mma_supports(dtype, d, group)) return PA_ERR_UNSUPPORTED;
   if (num_seqs > kMaxSeqs) return PA_ERR_UNSUPPORTED;
   // the largest element offset of a pool must fit the kernels' size_t math and
   // a page count times rows must fit the int64 row index (always true here)
@@ -81,6 +84,12 @@ pa::DecodeParams make_params(const void *q, const void *k_pool, const void *v_po
 }
 
 pa_status launched(cudaError_t err) { return err == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
+
+// f16/bf16 rows the tensor-core kernel covers go there; the rest to the CUDA cores.
+cudaError_t launch_read(const pa::DecodeParams &p, pa_dtype dtype, cudaStream_t stream) {
+  if (pa::mma_supports(dtype, p.head_dim, p.group)) return pa::launch_decode_mma(p, dtype, stream);
+  return pa::launch_decode_simt(p, dtype, stream);
+}
 
 }  // namespace
 
@@ -162,7 +171,7 @@ pa_status pa_decode(void *out, const void *q, const void *k_pool, const void *v_
   p.out = out;
   p.pages_per_split = 0;
   p.num_splits = 1;
-  return launched(pa::launch_decode_simt(p, dtype, reinterpret_cast<cudaStream_t>(stream)));
+  return launched(launch_read(p, dtype, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 pa_status pa_decode_splitkv(float *partial_out, float *partial_lse, const void *q,
@@ -191,7 +200,7 @@ pa_status pa_decode_splitkv(float *partial_out, float *partial_lse, const void *
   p.partial_lse = partial_lse;
   p.pages_per_split = pages_per_split;
   p.num_splits = max_splits;
-  return launched(pa::launch_decode_simt(p, dtype, reinterpret_cast<cudaStream_t>(stream)));
+  return launched(launch_read(p, dtype, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 pa_status pa_merge(void *out, const float *partial_out, const float *partial_lse,

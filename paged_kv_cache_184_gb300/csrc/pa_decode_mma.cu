@@ -1,0 +1,430 @@
+// Paged decode attention on the tensor cores (mma.sync m16n8k16), f16/bf16.
+//
+// Same contract as the CUDA-core read: one CTA per (sequence, kv head,
+// split); the block-table walk and the online softmax follow
+// "triton-attention-kernels" section "3. Paged KV-cache attention" and
+// nanoserve "Day 23: the real triton.jit paged-attention kernel".  What is
+// different is how one 16-token tile is reduced.  The tile is the M side of
+// two small matrix products, the GQA group of query heads is the N side:
+//
+//   S^T [16 tokens x 8 heads] = K_tile [16 x D] . Q^T [D x 8 heads]
+//   O^T [D x 8 heads]        += V_tile^T [D x 16] . P^T [16 x 8 heads]
+//
+// K feeds the first product through ldmatrix, V the second through
+// ldmatrix.trans; the probabilities P^T leave the first product's
+// accumulators and enter the second as a B operand after one movmatrix
+// transpose per 8x8 block, so scores never touch shared memory.  A group
+// of up to 8 heads fills one n8 tile, up to 16 heads two.
+//
+// Every warp owns every NW-th tile of the CTA's token range and streams it
+// through its own NS-stage cp.async ring (no CTA barrier in the main loop);
+// the warps' (m, l, O) states are combined once at the end.  Rows are stored
+// with a 16-byte-chunk XOR swizzle so that ldmatrix is bank-conflict free.
+// Tokens past the end of the range are zero-filled by the copy and masked
+// to -inf in the scores.
+#include <math_constants.h>
+
+#include "pa_common.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kTile = 16;  // tokens per tile (the mma M dimension)
+
+template <typename T> struct MmaT;
+template <> struct MmaT<__nv_bfloat16> {
+  __device__ __forceinline__ static void mma(float *d, const uint32_t *a, const uint32_t *b) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+  }
+  __device__ __forceinline__ static uint32_t pack(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+  }
+};
+template <> struct MmaT<__half> {
+  __device__ __forceinline__ static void mma(float *d, const uint32_t *a, const uint32_t *b) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+  }
+  __device__ __forceinline__ static uint32_t pack(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+  }
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t *r, uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t *r, uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// Compile-time shape of one instantiation.
+template <int D, int NT>
+struct Shape {
+  static constexpr int kSteps = D / 16;               // k-steps of S^T, m-tiles of O^T
+  static constexpr int kChunks = D / 8;               // 16-byte chunks in a row
+  static constexpr int kPitchChunks = (kChunks + 7) / 8 * 8;
+  static constexpr int kPitch = kPitchChunks * 16;    // bytes per smem row
+  static constexpr int kTileBytes = kTile * kPitch;   // one K (or V) tile
+  static constexpr int kStages = D <= 128 ? 3 : 2;
+  static constexpr int kStageBytes = 2 * kTileBytes;  // K then V
+  static constexpr int kWarpBytes = kStages * kStageBytes;
+  static constexpr int kHeads = 8 * NT;               // padded group size
+  static constexpr int kRingBytes = kWarps * kWarpBytes;
+  static constexpr int kCombineBytes = kWarps * kHeads * (D + 2) * 4;
+  static constexpr int kSmemBytes = kRingBytes > kCombineBytes ? kRingBytes : kCombineBytes;
+};
+
+// byte offset of (row, chunk) inside a tile: chunks XOR-swizzled by row
+template <int D, int NT>
+__device__ __forceinline__ uint32_t tile_off(int row, int chunk) {
+  return row * Shape<D, NT>::kPitch + ((chunk ^ (row & 7)) << 4);
+}
+
+template <typename T, int D, int NT>
+__global__ void __launch_bounds__(kThreads)
+    decode_mma_kernel(const DecodeParams p) {
+  using S = Shape<D, NT>;
+  using M = MmaT<T>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ int s_bad;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int r = lane >> 2;  // fragment row group
+  const int c = lane & 3;   // fragment column pair
+
+  const int hkv = p.num_kv_heads;
+  const int g = blockIdx.x % hkv;
+  const int split = blockIdx.x / hkv;
+  const int b = blockIdx.y;
+  const int G = p.group;
+  const int bs_log2 = p.block_size_log2;
+  const int bs_mask = (1 << bs_log2) - 1;
+
+  if (tid == 0) s_bad = 0;
+
+  // ---- token range of this CTA -------------------------------------------
+  int len = p.seq_lens[b];
+  const long long cap = static_cast<long long>(p.max_blocks) << bs_log2;
+  const bool bad_len = (len < 0) || (static_cast<long long>(len) > cap);
+  if (bad_len) {
+    if (tid == 0) report_error(p.dev_err, PA_DEV_BAD_SEQ_LEN);
+    len = 0;
+  }
+  int t_begin = 0, t_end = len;
+  if (p.pages_per_split > 0) {
+    const long long span = static_cast<long long>(p.pages_per_split) << bs_log2;
+    const long long lo = static_cast<long long>(split) * span;
+    t_begin = static_cast<int>(min(static_cast<long long>(len), lo));
+    t_end = static_cast<int>(min(static_cast<long long>(len), lo + span));
+  }
+
+  // ---- Q^T as mma B fragments: lane holds head r, dims 2c,2c+1 (+8) ------
+  uint32_t qb[NT][S::kSteps][2];
+  {
+    const T *qrow = static_cast<const T *>(p.q) +
+                    (static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(g) * G) * D;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int h = nt * 8 + r;
+#pragma unroll
+      for (int ks = 0; ks < S::kSteps; ++ks) {
+        if (h < G) {
+          const T *src = qrow + h * D + ks * 16 + 2 * c;
+          qb[nt][ks][0] = *reinterpret_cast<const uint32_t *>(src);
+          qb[nt][ks][1] = *reinterpret_cast<const uint32_t *>(src + 8);
+        } else {
+          qb[nt][ks][0] = 0u;
+          qb[nt][ks][1] = 0u;
+        }
+      }
+    }
+  }
+
+  const int32_t *bt_row = p.block_table + static_cast<size_t>(b) * p.max_blocks;
+  const T *kpool = static_cast<const T *>(p.k_pool);
+  const T *vpool = static_cast<const T *>(p.v_pool);
+  unsigned char *ring = smem + warp * S::kWarpBytes;
+  const uint32_t ring_u32 = smem_u32(ring);
+  __syncthreads();  // s_bad initialised
+
+  const int ntok = t_end - t_begin;
+  const int ntiles = ntok > 0 ? (ntok + kTile - 1) / kTile : 0;
+  // this warp's tiles: warp, warp + kWarps, ...
+  const int my_tiles = ntiles > warp ? (ntiles - warp + kWarps - 1) / kWarps : 0;
+
+  // issue the copies of this warp's i-th tile into stage `stage`
+  auto load_tile = [&](int i, int stage) {
+    const int tok0 = t_begin + (warp + i * kWarps) * kTile;
+    unsigned char *ks = ring + stage * S::kStageBytes;
+    unsigned char *vs = ks + S::kTileBytes;
+#pragma unroll
+    for (int q = lane; q < kTile * S::kChunks; q += 32) {
+      const int row = q / S::kChunks;
+      const int chunk = q - row * S::kChunks;
+      const int pos = tok0 + row;
+      bool valid = pos < t_end;
+      const T *ksrc = kpool;
+      const T *vsrc = vpool;
+      if (valid) {
+        const int page = bt_row[pos >> bs_log2];
+        if (page < 0 || page >= p.num_pages) {
+          report_error(p.dev_err, PA_DEV_BAD_PAGE);
+          s_bad = 1;
+          valid = false;
+        } else {
+          const size_t prow = (static_cast<size_t>(page) << bs_log2) + (pos & bs_mask);
+          const size_t off = (prow * hkv + g) * D + chunk * 8;
+          ksrc += off;
+          vsrc += off;
+        }
+      }
+      const uint32_t o = tile_off<D, NT>(row, chunk);
+      cp_async16(ks + o, ksrc, valid);
+      cp_async16(vs + o, vsrc, valid);
+    }
+  };
+
+#pragma unroll
+  for (int s = 0; s < S::kStages - 1; ++s) {
+    if (s < my_tiles) load_tile(s, s);
+    cp_async_commit();
+  }
+
+  // running state: heads 2c, 2c+1 of every n-tile
+  float m[NT][2], l[NT][2];
+  float o[S::kSteps][NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    m[nt][0] = m[nt][1] = -CUDART_INF_F;
+    l[nt][0] = l[nt][1] = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < S::kSteps; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[mt][nt][e] = 0.f;
+  }
+  const float sl2 = p.scale_log2;
+
+  for (int i = 0; i < my_tiles; ++i) {
+    cp_async_wait<S::kStages - 2>();
+    __syncwarp();
+    {
+      const int ni = i + S::kStages - 1;
+      if (ni < my_tiles) load_tile(ni, ni % S::kStages);
+      cp_async_commit();
+    }
+    const int stage = i % S::kStages;
+    const uint32_t ks_u32 = ring_u32 + stage * S::kStageBytes;
+    const uint32_t vs_u32 = ks_u32 + S::kTileBytes;
+    const int tok0 = t_begin + (warp + i * kWarps) * kTile;
+
+    // S^T = K . Q^T  (rows: tokens r, r+8; columns: heads 2c, 2c+1)
+    float sc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < S::kSteps; ++ks) {
+      // matrices: (tok 0-7, d lo), (tok 8-15, d lo), (tok 0-7, d hi), (tok 8-15, d hi)
+      const int mi = lane >> 3;
+      const int row = ((mi & 1) << 3) + (lane & 7);
+      const int chunk = ks * 2 + (mi >> 1);
+      uint32_t a[4];
+      ldsm_x4(a, ks_u32 + tile_off<D, NT>(row, chunk));
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) M::mma(sc[nt], a, qb[nt][ks]);
+    }
+
+    // online softmax over this tile, per head column
+    const bool v0 = tok0 + r < t_end;
+    const bool v1 = tok0 + r + 8 < t_end;
+    float alpha[NT][2];
+    uint32_t pb[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float s0 = v0 ? sc[nt][0] * sl2 : -CUDART_INF_F;  // token r,   head 2c
+      float s1 = v0 ? sc[nt][1] * sl2 : -CUDART_INF_F;  // token r,   head 2c+1
+      float s2 = v1 ? sc[nt][2] * sl2 : -CUDART_INF_F;  // token r+8, head 2c
+      float s3 = v1 ? sc[nt][3] * sl2 : -CUDART_INF_F;  // token r+8, head 2c+1
+      float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
+      const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
+      const float mu0 = mn0 == -CUDART_INF_F ? 0.f : mn0;
+      const float mu1 = mn1 == -CUDART_INF_F ? 0.f : mn1;
+      alpha[nt][0] = exp2f(m[nt][0] - mu0);
+      alpha[nt][1] = exp2f(m[nt][1] - mu1);
+      m[nt][0] = mn0;
+      m[nt][1] = mn1;
+      const float p0 = exp2f(s0 - mu0), p1 = exp2f(s1 - mu1);
+      const float p2 = exp2f(s2 - mu0), p3 = exp2f(s3 - mu1);
+      l[nt][0] = fmaf(l[nt][0], alpha[nt][0], p0 + p2);
+      l[nt][1] = fmaf(l[nt][1], alpha[nt][1], p1 + p3);
+      // P^T blocks (tokens 0-7 | 8-15) x heads, transposed into B fragments
+      pb[nt][0] = movmatrix_trans(M::pack(p0, p1));
+      pb[nt][1] = movmatrix_trans(M::pack(p2, p3));
+    }
+
+    // O^T = alpha * O^T + V^T . P^T
+#pragma unroll
+    for (int mt = 0; mt < S::kSteps; ++mt) {
+      // matrices of V^T: (d lo, tok 0-7), (d hi, tok 0-7), (d lo, tok 8-15), (d hi, tok 8-15)
+      const int mi = lane >> 3;
+      const int row = ((mi >> 1) << 3) + (lane & 7);
+      const int chunk = mt * 2 + (mi & 1);
+      uint32_t a[4];
+      ldsm_x4_trans(a, vs_u32 + tile_off<D, NT>(row, chunk));
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        o[mt][nt][0] *= alpha[nt][0];
+        o[mt][nt][1] *= alpha[nt][1];
+        o[mt][nt][2] *= alpha[nt][0];
+        o[mt][nt][3] *= alpha[nt][1];
+        M::mma(o[mt][nt], a, pb[nt]);
+      }
+    }
+  }
+  cp_async_wait_all();
+
+  // per-lane partial sums of l cover tokens r, r+8 only: finish them
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l[nt][0] += __shfl_xor_sync(0xffffffffu, l[nt][0], off);
+      l[nt][1] += __shfl_xor_sync(0xffffffffu, l[nt][1], off);
+    }
+  __syncthreads();  // every warp done with its ring: reuse smem for the combine
+
+  float *sm_m = reinterpret_cast<float *>(smem);          // [warp][head]
+  float *sm_l = sm_m + kWarps * S::kHeads;                 // [warp][head]
+  float *sm_o = sm_l + kWarps * S::kHeads;                 // [warp][head][D]
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int h0 = nt * 8 + 2 * c;
+    if (r == 0) {
+      sm_m[warp * S::kHeads + h0] = m[nt][0];
+      sm_m[warp * S::kHeads + h0 + 1] = m[nt][1];
+      sm_l[warp * S::kHeads + h0] = l[nt][0];
+      sm_l[warp * S::kHeads + h0 + 1] = l[nt][1];
+    }
+#pragma unroll
+    for (int mt = 0; mt < S::kSteps; ++mt) {
+      const int d0 = mt * 16 + r;
+      float *ob = sm_o + (warp * S::kHeads + h0) * D;
+      ob[d0] = o[mt][nt][0];
+      ob[D + d0] = o[mt][nt][1];
+      ob[d0 + 8] = o[mt][nt][2];
+      ob[D + d0 + 8] = o[mt][nt][3];
+    }
+  }
+  __syncthreads();
+
+  const bool bad = bad_len || (s_bad != 0);
+  const bool is_split = p.pages_per_split > 0;
+  for (int idx = tid; idx < G * D; idx += kThreads) {
+    const int h = idx / D;
+    const int d = idx - h * D;
+    float Mx = -CUDART_INF_F;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) Mx = fmaxf(Mx, sm_m[w * S::kHeads + h]);
+    float L = 0.f, O = 0.f;
+    if (Mx != -CUDART_INF_F) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float wgt = exp2f(sm_m[w * S::kHeads + h] - Mx);
+        L = fmaf(sm_l[w * S::kHeads + h], wgt, L);
+        O = fmaf(sm_o[(w * S::kHeads + h) * D + d], wgt, O);
+      }
+    }
+    const bool empty = bad || (Mx == -CUDART_INF_F);
+    const float res = empty ? 0.f : O / L;
+    const size_t qh = static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(g) * G + h;
+    if (is_split) {
+      const size_t row = qh * p.num_splits + split;
+      p.partial_out[row * D + d] = res;
+      if (d == 0)
+        p.partial_lse[row] = empty ? -CUDART_INF_F : (Mx + log2f(L)) * 0.69314718055994531f;
+    } else {
+      static_cast<T *>(p.out)[qh * D + d] = cvt_out<T>(res);
+    }
+  }
+}
+
+template <typename T, int D, int NT>
+cudaError_t launch_shape(const DecodeParams &p, cudaStream_t stream) {
+  using S = Shape<D, NT>;
+  auto kern = decode_mma_kernel<T, D, NT>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         S::kSmemBytes);
+  if (err != cudaSuccess) return err;
+  dim3 grid(p.num_splits * p.num_kv_heads, p.num_seqs);
+  kern<<<grid, kThreads, S::kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t launch_d(const DecodeParams &p, cudaStream_t stream) {
+  if (p.group <= 8) return launch_shape<T, D, 1>(p, stream);
+  return launch_shape<T, D, 2>(p, stream);
+}
+
+template <typename T>
+cudaError_t launch_typed(const DecodeParams &p, cudaStream_t stream) {
+  switch (p.head_dim) {
+    case 32: return launch_d<T, 32>(p, stream);
+    case 48: return launch_d<T, 48>(p, stream);
+    case 64: return launch_d<T, 64>(p, stream);
+    case 96: return launch_d<T, 96>(p, stream);
+    case 128: return launch_d<T, 128>(p, stream);
+    case 256: return launch_d<T, 256>(p, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+bool mma_supports(pa_dtype dtype, int head_dim, int group) {
+  if (dtype != PA_F16 && dtype != PA_BF16) return false;
+  if (group > 16) return false;
+  switch (head_dim) {
+    case 32: case 48: case 64: case 96: case 128: case 256: return true;
+  }
+  return false;
+}
+
+cudaError_t launch_decode_mma(const DecodeParams &p, pa_dtype dtype, cudaStream_t stream) {
+  if (dtype == PA_BF16) return launch_typed<__nv_bfloat16>(p, stream);
+  if (dtype == PA_F16) return launch_typed<__half>(p, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pa

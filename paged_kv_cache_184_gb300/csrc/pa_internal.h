@@ -44,7 +44,11 @@ struct MergeParams {
   int32_t num_splits, head_dim;
 };
 
+// CUDA-core read: every dtype, query groups of up to 8 heads.
 cudaError_t launch_decode_simt(const DecodeParams &p, pa_dtype dtype, cudaStream_t stream);
+// Tensor-core read: f16/bf16, head_dim in {32, 48, 64, 96, 128, 256}, groups of up to 16.
+bool mma_supports(pa_dtype dtype, int head_dim, int group);
+cudaError_t launch_decode_mma(const DecodeParams &p, pa_dtype dtype, cudaStream_t stream);
 cudaError_t launch_append(const AppendParams &p, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams &p, pa_dtype dtype, cudaStream_t stream);
 

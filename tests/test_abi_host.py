@@ -67,6 +67,9 @@ def _decode(raw, **kw):
     (dict(d=512), pa.PA_ERR_UNSUPPORTED),                # beyond 256
     (dict(d=6, dt=pa.PA_F32), pa.PA_ERR_UNSUPPORTED),    # 24 bytes
     (dict(hq=18, hkv=1), pa.PA_ERR_UNSUPPORTED),         # group of 18
+    (dict(hq=12, hkv=1, dt=pa.PA_F32), pa.PA_ERR_UNSUPPORTED),   # group 12 needs f16/bf16
+    (dict(hq=12, hkv=1, d=80), pa.PA_ERR_UNSUPPORTED),   # ... and a tensor-core head_dim
+    (dict(hq=16, hkv=1, b=0), pa.PA_OK),                 # group 16, bf16, d 64
     (dict(bs=12), pa.PA_ERR_INVALID_ARG),                # not a power of two
     (dict(bs=0), pa.PA_ERR_INVALID_ARG),
     (dict(bs=2048), pa.PA_ERR_UNSUPPORTED),

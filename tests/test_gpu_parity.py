@@ -203,11 +203,20 @@ def test_zero_length_sequence_gives_zero(lib):
 
 
 @pytest.mark.parametrize("dtype,hq,hkv,d,bs", [
+    # CUDA-core read
     ("f32", 8, 8, 256, 16),     # two chunks per lane, group 1
-    ("bf16", 16, 2, 128, 1),    # one token per page, group 8
     ("f16", 6, 3, 16, 64),      # tiny rows (two chunks), group 2, big pages
-    ("bf16", 40, 8, 96, 32),    # group 5
     ("f32", 4, 1, 48, 8),       # group 4, 12 chunks per row
+    ("bf16", 8, 4, 80, 16),     # head_dim outside the tensor-core list
+    ("f32", 16, 2, 64, 16),     # group 8
+    # tensor-core read
+    ("bf16", 16, 2, 128, 1),    # one token per page, group 8
+    ("bf16", 40, 8, 96, 32),    # group 5
+    ("f16", 48, 4, 64, 16),     # group 12: two head tiles
+    ("bf16", 32, 2, 128, 8),    # group 16, pages smaller than a tile
+    ("bf16", 4, 4, 32, 4),      # group 1
+    ("f16", 8, 2, 256, 16),     # widest rows
+    ("bf16", 6, 2, 48, 2),      # group 3, head_dim 48
 ])
 def test_decode_other_shapes(lib, dtype, hq, hkv, d, bs):
     lens = [1, bs - 1 if bs > 1 else 2, 3 * bs + 5, 700]
