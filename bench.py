@@ -299,7 +299,7 @@ def main():
     rb = read_bytes(lens, g.num_q_heads, g.num_kv_heads, g.head_dim, elem, g.block_size)
     ab = append_bytes(g.num_seqs, g.num_kv_heads, g.head_dim, elem)
     step_bytes = rb + ab
-    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(torch, dev)
     small = args.history < 1024  # history too short to exceed L2 by itself
 
     def step():
@@ -324,7 +324,7 @@ def main():
     barrier()
     for k in range(args.steps):
         if small:
-            flush.zero_()
+            flush()
         ev[k][0].record(stream)
         pa.pa_cache_append(g.k_new, g.v_new, g.k_pool, g.v_pool, g.block_table, g.positions,
                            dev_err=err)
@@ -370,7 +370,7 @@ def main():
     e0.record(stream)
     for _ in range(args.steps):
         if small:
-            flush.zero_()
+            flush()
         e2e_step()
     e1.record(stream)
     barrier()
@@ -414,6 +414,19 @@ def main():
         dist.destroy_process_group()
 
 
+class L2Flush:
+    """Evicts L2 by reading a buffer twice its size.  Reading (not writing)
+    leaves no dirty lines behind, so the next kernel pays no write-back."""
+
+    def __init__(self, torch, dev):
+        self.buf = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+        self.sink = torch.empty((), dtype=torch.float32, device=dev)
+        self.torch = torch
+
+    def __call__(self):
+        self.torch.sum(self.buf, dim=0, out=self.sink)
+
+
 def _time_launches(fn, torch, flush, iters=30, warm=3):
     """Median / min device time (ms) of fn over iters launches, L2 flushed before each."""
     stream = torch.cuda.current_stream()
@@ -421,7 +434,7 @@ def _time_launches(fn, torch, flush, iters=30, warm=3):
         fn()
     ts = []
     for _ in range(iters):
-        flush.zero_()
+        flush()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         fn()
@@ -449,7 +462,7 @@ def sweep(pa, workloads, torch, dev, flush, peak):
 
 def longctx(pa, workloads, torch, dev, peak):
     rows = []
-    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(torch, dev)
     for h in workloads.LONGCTX_HISTORIES:
         g = workloads.longctx(h, device=str(dev))
         s = pa.pa_num_splits(g.max_blocks, g.pages_per_split)
@@ -476,7 +489,7 @@ def longctx(pa, workloads, torch, dev, peak):
 
 
 def ragged(pa, workloads, torch, dev, peak):
-    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(torch, dev)
     g = workloads.ragged8b(device=str(dev))
     out = torch.empty_like(g.q)
     s = pa.pa_num_splits(g.max_blocks, 64)

@@ -15,6 +15,8 @@ namespace {
 constexpr int kThreads = 256;
 
 __global__ void __launch_bounds__(kThreads) append_kernel(const AppendParams p) {
+  pdl_trigger();  // the read that follows may launch now; it waits for this grid
+  pdl_wait();
   const long long gid = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x;
   const long long total = static_cast<long long>(p.num_tokens) * p.row_chunks;
   if (gid >= total) return;
@@ -52,8 +54,8 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendParams p) 
 cudaError_t launch_append(const AppendParams &p, cudaStream_t stream) {
   const long long total = static_cast<long long>(p.num_tokens) * p.row_chunks;
   const long long blocks = (total + kThreads - 1) / kThreads;
-  append_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(append_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, stream,
+                    p);
 }
 
 }  // namespace pa

@@ -8,6 +8,16 @@
 
 namespace pa {
 
+// Programmatic dependent launch: a kernel launched with the
+// programmatic-stream-serialization attribute may start while the kernel
+// before it in the stream is finishing; pdl_wait() blocks until that kernel
+// has completed and its writes are visible (a no-op when there is none).
+// pdl_trigger() lets the next kernel in the stream start its launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 // Record the first device-side error of a launch (first writer wins).
 __device__ __forceinline__ void report_error(int32_t *dev_err, int32_t code) {
   if (dev_err != nullptr) atomicCAS(dev_err, 0, code);

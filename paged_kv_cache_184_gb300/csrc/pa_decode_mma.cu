@@ -30,7 +30,21 @@
 namespace pa {
 namespace {
 
-constexpr int kWarps = 4;
+// Ring shape: warps per CTA and copy stages per warp (smem per CTA is
+// warps x stages x 2 tiles).  At head_dim 64, 4 warps x 3 stages = 48 KB
+// keeps 4 CTAs per SM, so 64 sequences x 8 kv heads run in one wave; at
+// head_dim 128, 2 stages (64 KB, 3 CTAs per SM) measured faster than 3.
+#ifndef PA_MMA_WARPS
+#define PA_MMA_WARPS 4
+#endif
+#ifndef PA_MMA_STAGES_D64   // head_dim <= 64
+#define PA_MMA_STAGES_D64 3
+#endif
+#ifndef PA_MMA_STAGES_D128  // 64 < head_dim <= 128
+#define PA_MMA_STAGES_D128 2
+#endif
+
+constexpr int kWarps = PA_MMA_WARPS;
 constexpr int kThreads = kWarps * 32;
 constexpr int kTile = 16;  // tokens per tile (the mma M dimension)
 
@@ -88,7 +102,7 @@ struct Shape {
   static constexpr int kPitchChunks = (kChunks + 7) / 8 * 8;
   static constexpr int kPitch = kPitchChunks * 16;    // bytes per smem row
   static constexpr int kTileBytes = kTile * kPitch;   // one K (or V) tile
-  static constexpr int kStages = D <= 128 ? 3 : 2;
+  static constexpr int kStages = D <= 64 ? PA_MMA_STAGES_D64 : D <= 128 ? PA_MMA_STAGES_D128 : 2;
   static constexpr int kStageBytes = 2 * kTileBytes;  // K then V
   static constexpr int kWarpBytes = kStages * kStageBytes;
   static constexpr int kHeads = 8 * NT;               // padded group size
@@ -126,22 +140,23 @@ __global__ void __launch_bounds__(kThreads)
   const int bs_mask = (1 << bs_log2) - 1;
 
   if (tid == 0) s_bad = 0;
+  pdl_wait();
 
-  // ---- token range of this CTA -------------------------------------------
-  int len = p.seq_lens[b];
+  // The prologue issues its independent loads together: the length, q, and
+  // the page ids of this warp's first tiles (read speculatively from the
+  // split's first position, index clamped inside the row, validated below).
+  const int32_t *bt_row = p.block_table + static_cast<size_t>(b) * p.max_blocks;
   const long long cap = static_cast<long long>(p.max_blocks) << bs_log2;
-  const bool bad_len = (len < 0) || (static_cast<long long>(len) > cap);
-  if (bad_len) {
-    if (tid == 0) report_error(p.dev_err, PA_DEV_BAD_SEQ_LEN);
-    len = 0;
+  const long long span =
+      p.pages_per_split > 0 ? static_cast<long long>(p.pages_per_split) << bs_log2 : cap;
+  const long long lo = p.pages_per_split > 0 ? static_cast<long long>(split) * span : 0;
+  int pid_pre[S::kStages];
+#pragma unroll
+  for (int s = 0; s < S::kStages; ++s) {
+    const long long pos = lo + (warp + s * kWarps) * kTile + (lane & (kTile - 1));
+    pid_pre[s] = __ldg(bt_row + ((pos < cap ? pos : cap - 1) >> bs_log2));
   }
-  int t_begin = 0, t_end = len;
-  if (p.pages_per_split > 0) {
-    const long long span = static_cast<long long>(p.pages_per_split) << bs_log2;
-    const long long lo = static_cast<long long>(split) * span;
-    t_begin = static_cast<int>(min(static_cast<long long>(len), lo));
-    t_end = static_cast<int>(min(static_cast<long long>(len), lo + span));
-  }
+  int len = __ldg(p.seq_lens + b);
 
   // ---- Q^T as mma B fragments: lane holds head r, dims 2c,2c+1 (+8) ------
   uint32_t qb[NT][S::kSteps][2];
@@ -155,8 +170,8 @@ __global__ void __launch_bounds__(kThreads)
       for (int ks = 0; ks < S::kSteps; ++ks) {
         if (h < G) {
           const T *src = qrow + h * D + ks * 16 + 2 * c;
-          qb[nt][ks][0] = *reinterpret_cast<const uint32_t *>(src);
-          qb[nt][ks][1] = *reinterpret_cast<const uint32_t *>(src + 8);
+          qb[nt][ks][0] = __ldg(reinterpret_cast<const uint32_t *>(src));
+          qb[nt][ks][1] = __ldg(reinterpret_cast<const uint32_t *>(src + 8));
         } else {
           qb[nt][ks][0] = 0u;
           qb[nt][ks][1] = 0u;
@@ -165,7 +180,15 @@ __global__ void __launch_bounds__(kThreads)
     }
   }
 
-  const int32_t *bt_row = p.block_table + static_cast<size_t>(b) * p.max_blocks;
+  // ---- token range of this CTA -------------------------------------------
+  const bool bad_len = (len < 0) || (static_cast<long long>(len) > cap);
+  if (bad_len) {
+    if (tid == 0) report_error(p.dev_err, PA_DEV_BAD_SEQ_LEN);
+    len = 0;
+  }
+  const int t_begin = static_cast<int>(min(static_cast<long long>(len), lo));
+  const int t_end = static_cast<int>(min(static_cast<long long>(len), lo + span));
+
   const T *kpool = static_cast<const T *>(p.k_pool);
   const T *vpool = static_cast<const T *>(p.v_pool);
   unsigned char *ring = smem + warp * S::kWarpBytes;
@@ -177,8 +200,17 @@ __global__ void __launch_bounds__(kThreads)
   // this warp's tiles: warp, warp + kWarps, ...
   const int my_tiles = ntiles > warp ? (ntiles - warp + kWarps - 1) / kWarps : 0;
 
-  // issue the copies of this warp's i-th tile into stage `stage`
-  auto load_tile = [&](int i, int stage) {
+  // Page id of token (lane & 15) of this warp's i-th tile (-1 past the end).
+  // Fetched one tile ahead of its copies, so the block-table load never sits
+  // between a wait and the next copy issue.
+  auto fetch_pid = [&](int i) -> int {
+    const int pos = t_begin + (warp + i * kWarps) * kTile + (lane & (kTile - 1));
+    return (i < my_tiles && pos < t_end) ? __ldg(bt_row + (pos >> bs_log2)) : -1;
+  };
+
+  // issue the copies of this warp's i-th tile into stage `stage`; lane j of
+  // the first 16 holds the page id of token j of the tile in `pid`
+  auto load_tile = [&](int i, int stage, int pid) {
     const int tok0 = t_begin + (warp + i * kWarps) * kTile;
     unsigned char *ks = ring + stage * S::kStageBytes;
     unsigned char *vs = ks + S::kTileBytes;
@@ -187,11 +219,11 @@ __global__ void __launch_bounds__(kThreads)
       const int row = q / S::kChunks;
       const int chunk = q - row * S::kChunks;
       const int pos = tok0 + row;
+      const int page = __shfl_sync(0xffffffffu, pid, row);
       bool valid = pos < t_end;
       const T *ksrc = kpool;
       const T *vsrc = vpool;
       if (valid) {
-        const int page = bt_row[pos >> bs_log2];
         if (page < 0 || page >= p.num_pages) {
           report_error(p.dev_err, PA_DEV_BAD_PAGE);
           s_bad = 1;
@@ -211,9 +243,10 @@ __global__ void __launch_bounds__(kThreads)
 
 #pragma unroll
   for (int s = 0; s < S::kStages - 1; ++s) {
-    if (s < my_tiles) load_tile(s, s);
+    if (s < my_tiles) load_tile(s, s, pid_pre[s]);
     cp_async_commit();
   }
+  int pid_next = pid_pre[S::kStages - 1];
 
   // running state: heads 2c, 2c+1 of every n-tile
   float m[NT][2], l[NT][2];
@@ -234,7 +267,10 @@ __global__ void __launch_bounds__(kThreads)
     __syncwarp();
     {
       const int ni = i + S::kStages - 1;
-      if (ni < my_tiles) load_tile(ni, ni % S::kStages);
+      if (ni < my_tiles) {
+        load_tile(ni, ni % S::kStages, pid_next);
+        pid_next = fetch_pid(ni + 1);
+      }
       cp_async_commit();
     }
     const int stage = i % S::kStages;
@@ -313,6 +349,7 @@ __global__ void __launch_bounds__(kThreads)
     }
   }
   cp_async_wait_all();
+  pdl_trigger();  // the merge (or the next read) may start launching
 
   // per-lane partial sums of l cover tokens r, r+8 only: finish them
 #pragma unroll
@@ -387,8 +424,7 @@ cudaError_t launch_shape(const DecodeParams &p, cudaStream_t stream) {
                                          S::kSmemBytes);
   if (err != cudaSuccess) return err;
   dim3 grid(p.num_splits * p.num_kv_heads, p.num_seqs);
-  kern<<<grid, kThreads, S::kSmemBytes, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(kThreads), S::kSmemBytes, stream, p);
 }
 
 template <typename T, int D>

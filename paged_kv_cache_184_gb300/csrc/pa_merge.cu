@@ -19,6 +19,7 @@ constexpr int kMaxPerLane = 8;  // head_dim <= 256
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads) merge_kernel(const MergeParams p) {
+  pdl_wait();  // the partials come from the split read just before
   const int row = blockIdx.x * kWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= p.rows) return;
@@ -71,12 +72,12 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const MergeParams p) {
 cudaError_t launch_merge(const MergeParams &p, pa_dtype dtype, cudaStream_t stream) {
   const unsigned blocks = static_cast<unsigned>((p.rows + kWarps - 1) / kWarps);
   switch (dtype) {
-    case PA_F32: merge_kernel<float><<<blocks, kThreads, 0, stream>>>(p); break;
-    case PA_F16: merge_kernel<__half><<<blocks, kThreads, 0, stream>>>(p); break;
-    case PA_BF16: merge_kernel<__nv_bfloat16><<<blocks, kThreads, 0, stream>>>(p); break;
-    default: return cudaErrorInvalidValue;
+    case PA_F32: return launch_pdl(merge_kernel<float>, dim3(blocks), dim3(kThreads), 0, stream, p);
+    case PA_F16: return launch_pdl(merge_kernel<__half>, dim3(blocks), dim3(kThreads), 0, stream, p);
+    case PA_BF16:
+      return launch_pdl(merge_kernel<__nv_bfloat16>, dim3(blocks), dim3(kThreads), 0, stream, p);
   }
-  return cudaGetLastError();
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace pa
