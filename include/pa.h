@@ -4,7 +4,7 @@
  * The cache is a fixed pool of pages.  A page holds block_size consecutive
  * tokens of one sequence; a sequence's block table lists its pages in order,
  * so token p of sequence b lives at slot p % block_size of page
- * block_table[b][p / block_size] ("triton-attention-kernels", section
+ * block_table[b][p / block_size] ("Three Attention Kernels", section
  * "3. Paged KV-cache attention": the page comes from the block table, the
  * row from the offset inside the page).
  *
@@ -113,7 +113,7 @@ pa_status pa_cache_append(const void *k_new, const void *v_new, void *k_pool,
  *   out[b][h] = softmax_t(scale * q[b][h] . K_b[t][g]) @ V_b[t][g],
  *   t = 0 .. seq_lens[b]-1,
  * where K_b[t] is read through the block table.  This is attention
- * softmax(Q K^T / sqrt(d)) V ("triton-attention-kernels", section "What is
+ * softmax(Q K^T / sqrt(d)) V ("Three Attention Kernels", section "What is
  * attention, really?") at decode (one query per sequence), computed in one
  * streaming pass with an online softmax (a running max and sum, the score
  * row never stored) as nanoserve "Day 23: the real triton.jit
@@ -133,7 +133,7 @@ pa_status pa_decode(void *out, const void *q, const void *k_pool,
 /*
  * pa_decode_splitkv - the same read, split along the history.
  *
- * "triton-attention-kernels", section "2. Split-KV flash-decoding": each
+ * "Three Attention Kernels", section "2. Split-KV flash-decoding": each
  * split reduces its own slice of K/V to a partial output and a log-sum-exp,
  * and a final cross-split combine (pa_merge) gives the output.  Here a split
  * is a fixed run of pages_per_split pages: split s of sequence b covers
@@ -159,7 +159,7 @@ pa_status pa_decode_splitkv(float *partial_out, float *partial_lse,
 /*
  * pa_merge - combine split partials into the output.
  *
- * "triton-attention-kernels", section "2. Split-KV flash-decoding", the
+ * "Three Attention Kernels", section "2. Split-KV flash-decoding", the
  * cross-SM combine: for every (b, h), M = max_s partial_lse[b][h][s],
  * w_s = exp(partial_lse[b][h][s] - M), and
  *   out[b][h] = sum_s w_s * partial_out[b][h][s] / sum_s w_s,

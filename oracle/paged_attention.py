@@ -7,11 +7,11 @@ CPU-baseline leg; the CUDA library never calls it.
 
 What it follows:
 
-* Attention itself: softmax(Q K^T / sqrt(d)) V ("triton-attention-kernels",
+* Attention itself: softmax(Q K^T / sqrt(d)) V ("Three Attention Kernels",
   section "What is attention, really?").  ``scale`` is passed explicitly.
 * Reading through a block table: the page of token p of sequence b is
   ``block_table[b][p // page_size]`` and the token sits at slot
-  ``p % page_size`` of that page ("triton-attention-kernels", section
+  ``p % page_size`` of that page ("Three Attention Kernels", section
   "3. Paged KV-cache attention").
 * The gather form: rebuild the contiguous history through the block table,
   then run ordinary attention over it (nanoserve "Day 20: the number the
@@ -20,7 +20,7 @@ What it follows:
 * Split-KV partials and their combine: every split reduces its own slice of
   the history to an output and a log-sum-exp; the combine takes the max
   lse, weights each split by exp(lse - max) and normalises by the sum of
-  weights ("triton-attention-kernels", section "2. Split-KV
+  weights ("Three Attention Kernels", section "2. Split-KV
   flash-decoding").
 * Cache append: "grow the table, scatter the K/V" (nanoserve Day 20,
   section "What I learned"); the table is grown by the caller, the scatter

@@ -2,7 +2,7 @@
 //
 // Same contract as the CUDA-core read: one CTA per (sequence, kv head,
 // split); the block-table walk and the online softmax follow
-// "triton-attention-kernels" section "3. Paged KV-cache attention" and
+// "Three Attention Kernels" section "3. Paged KV-cache attention" and
 // nanoserve "Day 23: the real triton.jit paged-attention kernel".  What is
 // different is how one 16-token tile is reduced.  The tile is the M side of
 // two small matrix products, the GQA group of query heads is the N side:

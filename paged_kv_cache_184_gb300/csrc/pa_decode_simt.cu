@@ -1,7 +1,7 @@
 // Paged decode attention on the CUDA cores (fp32 FMA), any supported dtype.
 //
 // One CTA per (sequence, kv head, split).  The CTA walks its token range of
-// the block table ("triton-attention-kernels", section "3. Paged KV-cache
+// the block table ("Three Attention Kernels", section "3. Paged KV-cache
 // attention": page = block_table[b][p / page_size], row = p % page_size),
 // streams K and V rows of its kv head through a 4-stage cp.async ring in
 // shared memory, and keeps an online softmax per query head (nanoserve

@@ -1,6 +1,6 @@
 // Cross-split combine of split-KV partials.
 //
-// "triton-attention-kernels", section "2. Split-KV flash-decoding": after
+// "Three Attention Kernels", section "2. Split-KV flash-decoding": after
 // every split reduced its slice, the outputs are combined with weights
 // exp(lse_s - max lse), normalised by their sum.  One warp per (sequence,
 // query head) row: lanes stride over the splits for the max and the

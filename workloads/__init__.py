@@ -7,7 +7,7 @@ CUDA path and the CPU oracle can take their inputs from here.
 
 Shapes follow the workloads the pages describe (nanoserve "Day 20: the
 number the Triton kernel has to beat" uses the Llama-3.2-1B head layout;
-"triton-attention-kernels", section "Benchmark method", sweeps contexts of
+"Three Attention Kernels", section "Benchmark method", sweeps contexts of
 1K to 16K).  Named configurations:
 
 * ``tiny``      : 1 sequence, history 64, Hq 32 / Hkv 8, d 64, fp32, pool 16.
