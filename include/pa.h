@@ -20,9 +20,10 @@
  * attention with contiguous groups).
  *
  * Ownership: every pointer is device memory owned by the caller.  The
- * library allocates no memory, keeps no state between calls, and launches
- * its kernels asynchronously on the caller's stream; the call returns once
- * the launch is queued.
+ * library allocates no memory and launches its kernels asynchronously on the
+ * caller's stream; the call returns once the launch is queued.  Apart from
+ * the fixed array behind pa_decode_splitkv_noalloc it keeps no state between
+ * calls.
  *
  * Errors: argument checks run on the host before any launch and return
  * PA_ERR_INVALID_ARG (a null or misaligned pointer, a negative or
@@ -170,6 +171,45 @@ pa_status pa_merge(void *out, const float *partial_out,
                    const float *partial_lse, int32_t num_seqs,
                    int32_t num_q_heads, int32_t max_splits, int32_t head_dim,
                    pa_dtype dtype, pa_stream_t stream);
+
+/* Size of the library-owned partials array behind pa_decode_splitkv_noalloc. */
+#define PA_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * pa_decode_splitkv_noalloc - split-KV read and merge without caller scratch.
+ *
+ * The pages have no counterpart to this call: it exists for callers that
+ * cannot allocate device memory, so cannot pass pa_decode_splitkv the space
+ * for its partial results.  Examples are a plugin whose host framework owns
+ * every device allocation and hands it only inputs and outputs, or a serving
+ * loop that must not call cudaMalloc/cudaFree because they may synchronize
+ * the device.  It computes what pa_decode_splitkv followed by pa_merge
+ * computes: out[b][h] for every sequence and query head, with
+ * splits = pa_num_splits(max_blocks_per_seq, pages_per_split).  The partials
+ * live in an array of PA_NOALLOC_SCRATCH_BYTES that the library places in
+ * device memory on every GPU that loads it, held until the process exits.
+ * The call allocates nothing.
+ *
+ * Limit: the partials take num_seqs * num_q_heads * splits * (head_dim + 1)
+ * floats (each part rounded up to 256 bytes).  A call that needs more than
+ * PA_NOALLOC_SCRATCH_BYTES returns PA_ERR_UNSUPPORTED and launches nothing.
+ * Other arguments are checked as in pa_decode_splitkv and pa_merge.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Call it with the device that owns the stream and the data
+ * current.  Every call on a device shares the one array.  Nothing depends on
+ * what an earlier call left there, but calls whose kernels overlap on the GPU
+ * (different streams, different host threads) race on it.
+ */
+pa_status pa_decode_splitkv_noalloc(void *out, const void *q, const void *k_pool,
+                                    const void *v_pool, const int32_t *block_table,
+                                    int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                                    int32_t num_seqs, int32_t num_q_heads,
+                                    int32_t num_kv_heads, int32_t head_dim,
+                                    int32_t block_size, int32_t num_pages, float scale,
+                                    int32_t pages_per_split, pa_dtype dtype,
+                                    int32_t *dev_err, pa_stream_t stream);
 
 #ifdef __cplusplus
 }

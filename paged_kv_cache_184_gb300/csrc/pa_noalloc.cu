@@ -1,0 +1,82 @@
+// pa_decode_splitkv_noalloc: the split-KV read and its merge in one call,
+// for callers that cannot allocate device memory.
+//
+// The split read needs somewhere to put its per-split partial outputs and
+// log-sum-exps before the merge combines them.  pa_decode_splitkv takes that
+// space from the caller.  Some callers have no way to provide it: a plugin
+// running inside a host framework that owns every device allocation (and
+// hands the plugin only its inputs and outputs), or a latency-critical
+// serving loop that must never call cudaMalloc/cudaFree because they can
+// synchronize the whole device.  This entry point keeps the partials in a
+// fixed array that the library itself places in device memory when it is
+// loaded, so a call allocates nothing.
+//
+// The array is shared by every call on a device and keeps whatever the last
+// call left in it.  Nothing here depends on its earlier contents: the split
+// read writes every partial (including -inf for empty splits) that the merge
+// then reads.  Two calls whose kernels overlap on the GPU (on different
+// streams, or from different host threads) use the same array and race.
+#include <atomic>
+
+#include "pa_internal.h"
+
+namespace {
+
+// Lives in device memory on every GPU that loads the library, until exit.
+__device__ __align__(256) unsigned char g_partials[PA_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 256;
+std::atomic<unsigned char *> g_partials_addr[kMaxDevices];
+
+// Device address of g_partials on the current device (looked up once per
+// device; in host code the symbol itself is only a host-side handle).
+cudaError_t partials_address(unsigned char **addr) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  unsigned char *p = g_partials_addr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
+    void *sym = nullptr;
+    err = cudaGetSymbolAddress(&sym, g_partials);
+    if (err != cudaSuccess) return err;
+    p = static_cast<unsigned char *>(sym);
+    g_partials_addr[dev].store(p, std::memory_order_release);
+  }
+  *addr = p;
+  return cudaSuccess;
+}
+
+int64_t align256(int64_t x) { return (x + 255) / 256 * 256; }
+
+}  // namespace
+
+extern "C" pa_status pa_decode_splitkv_noalloc(
+    void *out, const void *q, const void *k_pool, const void *v_pool, const int32_t *block_table,
+    int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t num_seqs, int32_t num_q_heads,
+    int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_pages, float scale,
+    int32_t pages_per_split, pa_dtype dtype, int32_t *dev_err, pa_stream_t stream) {
+  if (num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0 || pages_per_split <= 0 ||
+      max_blocks_per_seq <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (num_seqs == 0) return PA_OK;
+  const int32_t splits = pa_num_splits(max_blocks_per_seq, pages_per_split);
+  const int64_t rows = static_cast<int64_t>(num_seqs) * num_q_heads * splits;
+  const int64_t out_bytes = align256(rows * head_dim * static_cast<int64_t>(sizeof(float)));
+  const int64_t lse_bytes = align256(rows * static_cast<int64_t>(sizeof(float)));
+  if (out_bytes + lse_bytes > static_cast<int64_t>(PA_NOALLOC_SCRATCH_BYTES))
+    return PA_ERR_UNSUPPORTED;  // partials would not fit the fixed array
+
+  unsigned char *base = nullptr;
+  if (partials_address(&base) != cudaSuccess) return PA_ERR_CUDA;
+  float *partial_out = reinterpret_cast<float *>(base);
+  float *partial_lse = reinterpret_cast<float *>(base + out_bytes);
+
+  pa_status st = pa_decode_splitkv(partial_out, partial_lse, q, k_pool, v_pool, block_table,
+                                   max_blocks_per_seq, seq_lens, num_seqs, num_q_heads,
+                                   num_kv_heads, head_dim, block_size, num_pages, scale,
+                                   pages_per_split, splits, dtype, dev_err, stream);
+  if (st != PA_OK) return st;
+  return pa_merge(out, partial_out, partial_lse, num_seqs, num_q_heads, splits, head_dim, dtype,
+                  stream);
+}

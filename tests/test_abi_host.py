@@ -161,3 +161,20 @@ def test_binding_rejects_host_tensors(lib):
 def test_binding_raises_on_bad_status(lib):
     assert isinstance(pa.PaError("pa_decode", 2), RuntimeError)
     assert "PA_ERR_UNSUPPORTED" in str(pa.PaError("pa_decode", 2))
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(pps=0), pa.PA_ERR_INVALID_ARG),
+    (dict(b=-1), pa.PA_ERR_INVALID_ARG),
+    (dict(b=0), pa.PA_OK),
+    # 64 x 32 x 8192 splits x 65 floats: far beyond the fixed partials array
+    (dict(b=64, mb=8192, pps=1), pa.PA_ERR_UNSUPPORTED),
+])
+def test_noalloc_validation_before_any_device_call(lib, kw, want):
+    a = dict(out=FAKE, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, mb=10, sl=FAKE, b=2, hq=32, hkv=8, d=64,
+             bs=16, np_=32, scale=0.125, pps=4, dt=pa.PA_BF16)
+    a.update(kw)
+    st = lib.raw().pa_decode_splitkv_noalloc(
+        a["out"], a["q"], a["k"], a["v"], a["bt"], a["mb"], a["sl"], a["b"], a["hq"], a["hkv"],
+        a["d"], a["bs"], a["np_"], a["scale"], a["pps"], a["dt"], None, None)
+    assert st == want
