@@ -80,6 +80,24 @@ def split_bytes(b, hq, s, d):
     return 2 * b * hq * s * (d + 1) * 4
 
 
+# ----------------------------------------------------------------- ranks
+
+
+def max_over_ranks(dist, x: float, device) -> float:
+    """The largest x over all ranks (x itself when not distributed)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_rank_step: int, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank's bytes over the slowest rank's time."""
+    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+
+
 # ----------------------------------------------------------------- environment
 
 
@@ -282,13 +300,6 @@ def main():
             dist.barrier()
         torch.cuda.synchronize()
 
-    def max_over_ranks(x: float) -> float:
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
     # ------------------------------------------------ headline workload
     cpu = workloads.llama1b(args.history)
     g = cpu.to(dev)
@@ -334,10 +345,10 @@ def main():
     barrier()
     clk = clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    ms_per_step = max_over_ranks(sum(step_ms) / args.steps)
+    ms_per_step = max_over_ranks(dist, sum(step_ms) / args.steps, dev)
     if int(err.item()) != 0:
         raise RuntimeError(f"device error {int(err.item())} during the timed steps")
-    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    value = job_gbs(step_bytes, world, ms_per_step)
     gpu_launches = 2 * args.steps
 
     # the dominant kernel alone, same launch, K launches with an event pair each
@@ -394,8 +405,8 @@ def main():
         e2e_step()
     e1.record(stream)
     barrier()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
-    e2e_value = world * step_bytes / (e2e_ms * 1e-3) / 1e9
+    e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1) / args.steps, dev)
+    e2e_value = job_gbs(step_bytes, world, e2e_ms)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
