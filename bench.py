@@ -433,6 +433,7 @@ def main():
         line["sweep"] = sweep(pa, workloads, torch, dev, flush, peak)
         line["longctx"] = longctx(pa, workloads, torch, dev, peak)
         line["ragged8b"] = ragged(pa, workloads, torch, dev, peak)
+        line["dense_vs_sdpa"] = dense_vs_sdpa(pa, workloads, torch, dev, peak)
         if world == 1:
             t, nb, n = OracleSample(cpu).run(12.0, 64)
             line["cpu_baseline"] = {
@@ -544,6 +545,46 @@ def ragged(pa, workloads, torch, dev, peak):
     del g, out, po, pl
     torch.cuda.empty_cache()
     return res
+
+
+def dense_vs_sdpa(pa, workloads, torch, dev, peak):
+    """Contiguous K/V (B 4, H 16, D 64, fp16) at 1K-16K: our read at every split count of
+    the "Three Attention Kernels" sweep against torch SDPA on its own [B,H,N,D] layout."""
+    flush = L2Flush(torch, dev)
+    rows = []
+    for n in workloads.DENSE_CONTEXTS:
+        g = workloads.dense(n, device=str(dev))
+        out = torch.empty_like(g.q)
+        kvb = g.kv_bytes()
+        ours = {}
+        for splits in workloads.DENSE_SPLITS:
+            if splits == 1:
+                fn = lambda: pa.pa_decode(out, g.q, g.k_pool, g.v_pool, g.block_table,
+                                          g.seq_lens, g.scale)
+            else:
+                pps = g.max_blocks // splits
+                s = pa.pa_num_splits(g.max_blocks, pps)
+                po = torch.empty((4, 16, s, 64), device=dev)
+                pl = torch.empty((4, 16, s), device=dev)
+
+                def fn(po=po, pl=pl, pps=pps):
+                    pa.pa_decode_splitkv(po, pl, g.q, g.k_pool, g.v_pool, g.block_table,
+                                         g.seq_lens, g.scale, pps)
+                    pa.pa_merge(out, po, pl)
+            ours[splits] = 1e3 * _time_launches(fn, torch, flush, iters=20)[0]
+        k = g.k_pool.reshape(4, n, 16, 64).transpose(1, 2).contiguous()
+        v = g.v_pool.reshape(4, n, 16, 64).transpose(1, 2).contiguous()
+        q4 = g.q.unsqueeze(2)
+        sdpa = lambda: torch.nn.functional.scaled_dot_product_attention(q4, k, v, scale=g.scale)
+        t_sdpa = 1e3 * _time_launches(sdpa, torch, flush, iters=20)[0]
+        best = min(ours, key=ours.get)
+        rows.append({"n_ctx": n, "us_by_splits": {str(k_): round(v_, 2) for k_, v_ in ours.items()},
+                     "best_splits": best, "us_best": ours[best], "us_sdpa": t_sdpa,
+                     "gbs_best": kvb / (ours[best] * 1e-6) / 1e9,
+                     "gbs_sdpa": kvb / (t_sdpa * 1e-6) / 1e9, "sdpa_over_ours": t_sdpa / ours[best]})
+        del g, out, k, v
+    torch.cuda.empty_cache()
+    return rows
 
 
 if __name__ == "__main__":

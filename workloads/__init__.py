@@ -18,6 +18,11 @@ number the Triton kernel has to beat" uses the Llama-3.2-1B head layout;
                   d 128, bf16 with std 0.5, pool of 160,000 pages.
 * ``longctx``   : batch 8, history 32,768 or 131,072, Hq 32 / Hkv 8, d 128,
                   bf16, 1% of keys scaled by 8, 64-page KV splits.
+* ``dense``     : a contiguous (non-paged) cache, the shape of the split-KV
+                  benchmark of "Three Attention Kernels" ("Benchmark method":
+                  B 4, H 16, D 64, one query, fp16, contexts 1K to 16K).  The
+                  pool is the batch's K/V in order and the block table is the
+                  identity, so [B][N][H][D] memory is read as pages.
 
 Draw order is fixed: pool permutation, block tables, q, K pool, V pool,
 peaky-key mask, new K, new V.  K/V pools are drawn page-chunk by page-chunk
@@ -237,3 +242,28 @@ def longctx(history: int, batch: int = 8, device: str = "cpu") -> PagedBatch:
                       head_dim=128, block_size=16, num_pages=pages,
                       peaky_frac=0.01, peaky_factor=8.0, pages_per_split=64,
                       device=device)
+
+
+DENSE_CONTEXTS = (1024, 2048, 4096, 8192, 16384)
+DENSE_SPLITS = (1, 8, 16, 32, 64, 128)
+
+
+def dense(n_ctx: int, batch: int = 4, heads: int = 16, head_dim: int = 64,
+          dtype: str = "f16", device: str = "cpu", seed: int = 5) -> PagedBatch:
+    """Contiguous K/V: sequence b's pages are b*N/16 .. (b+1)*N/16 - 1, in order."""
+    bs = 16
+    npg = -(-n_ctx // bs)
+    tdtype = DTYPES[dtype]
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    table = torch.arange(batch * npg, dtype=torch.int32, device=device).reshape(batch, npg)
+    q = torch.randn((batch, heads, head_dim), generator=gen, device=device).to(tdtype)
+    k_pool = _draw_pool(gen, batch * npg, bs, heads, head_dim, 1.0, tdtype, device)
+    v_pool = _draw_pool(gen, batch * npg, bs, heads, head_dim, 1.0, tdtype, device)
+    k_new = torch.randn((batch, heads, head_dim), generator=gen, device=device).to(tdtype)
+    v_new = torch.randn((batch, heads, head_dim), generator=gen, device=device).to(tdtype)
+    seq_lens = torch.full((batch,), n_ctx, dtype=torch.int32, device=device)
+    return PagedBatch(name=f"dense_n{n_ctx}", q=q, k_pool=k_pool, v_pool=v_pool,
+                      block_table=table, seq_lens=seq_lens, k_new=k_new, v_new=v_new,
+                      positions=seq_lens - 1, scale=1.0 / math.sqrt(head_dim), block_size=bs,
+                      seed=seed, meta={"dense": True})
