@@ -434,6 +434,7 @@ def main():
         line["longctx"] = longctx(pa, workloads, torch, dev, peak)
         line["ragged8b"] = ragged(pa, workloads, torch, dev, peak)
         line["dense_vs_sdpa"] = dense_vs_sdpa(pa, workloads, torch, dev, peak)
+        line["chunk"] = chunk(pa, workloads, torch, dev, peak)
         if world == 1:
             t, nb, n = OracleSample(cpu).run(12.0, 64)
             line["cpu_baseline"] = {
@@ -547,6 +548,32 @@ def ragged(pa, workloads, torch, dev, peak):
     return res
 
 
+def chunk(pa, workloads, torch, dev, peak):
+    """Chunked multi-query read (pa_decode_chunk) on the llama1b batch at history 4096:
+    every sequence brings n_q queries (causal), K/V read once per (sequence, kv head)."""
+    flush = L2Flush(torch, dev)
+    g = workloads.llama1b(4096, device=str(dev))
+    rows = []
+    for n_q in (1, 4, 16, 64):
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(7)
+        q = torch.randn((64, n_q, 32, 64), generator=gen, device=dev).to(torch.bfloat16)
+        out = torch.empty_like(q)
+        fn = lambda: pa.pa_decode_chunk(out, q, g.k_pool, g.v_pool, g.block_table, g.seq_lens,
+                                        g.scale)
+        med, _ = _time_launches(fn, torch, flush, iters=20)
+        lens = g.lens_list()
+        kvb = read_bytes(lens, 32, 8, 64, 2, 16) + 2 * 64 * (n_q - 1) * 32 * 64 * 2
+        flops = sum(4 * 32 * 64 * (n - n_q + i + 1) for n in lens for i in range(n_q))
+        rows.append({"n_q": n_q, "us": 1e3 * med, "gbs": kvb / (med * 1e-3) / 1e9,
+                     "frac_hbm": kvb / (med * 1e-3) / 1e9 / peak,
+                     "tflops": flops / (med * 1e-3) / 1e12})
+        del q, out
+    del g
+    torch.cuda.empty_cache()
+    return rows
+
+
 def dense_vs_sdpa(pa, workloads, torch, dev, peak):
     """Contiguous K/V (B 4, H 16, D 64, fp16) at 1K-16K: our read at every split count of
     the "Three Attention Kernels" sweep against torch SDPA on its own [B,H,N,D] layout."""
@@ -562,7 +589,7 @@ def dense_vs_sdpa(pa, workloads, torch, dev, peak):
                 fn = lambda: pa.pa_decode(out, g.q, g.k_pool, g.v_pool, g.block_table,
                                           g.seq_lens, g.scale)
             else:
-                pps = g.max_blocks // splits
+                pps = max(1, g.max_blocks // splits)  # at least one page per split
                 s = pa.pa_num_splits(g.max_blocks, pps)
                 po = torch.empty((4, 16, s, 64), device=dev)
                 pl = torch.empty((4, 16, s), device=dev)

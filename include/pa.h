@@ -172,6 +172,30 @@ pa_status pa_merge(void *out, const float *partial_out,
                    int32_t num_q_heads, int32_t max_splits, int32_t head_dim,
                    pa_dtype dtype, pa_stream_t stream);
 
+/*
+ * pa_decode_chunk - causal read of a chunk of queries per sequence.
+ *
+ * nanoserve "Day 23: the real triton.jit paged-attention kernel": every
+ * query position i of a chunk is its own program, offset by the tokens
+ * already in the cache (past).  Each sequence b brings chunk_len queries
+ * whose K/V are already appended; seq_lens[b] counts the history and the
+ * chunk, so past = seq_lens[b] - chunk_len.  Query i sits at position
+ * past + i and attends to tokens 0 .. past + i:
+ *   out[b][i][h] = softmax_{t <= past+i}(scale * q[b][i][h] . K_b[t][g]) @ V_b[t][g].
+ * A query at a negative position (chunk_len > seq_lens[b]) sees nothing and
+ * its output is 0.  q and out are [num_seqs][chunk_len][num_q_heads][head_dim].
+ * chunk_len == 1 is a single-query read.  f16/bf16 only, head_dim 32, 48,
+ * 64, 96 or 128 (otherwise PA_ERR_UNSUPPORTED); fp32 accumulation and
+ * softmax, the probabilities rounded to the cache dtype for the P.V product.
+ */
+pa_status pa_decode_chunk(void *out, const void *q, const void *k_pool,
+                          const void *v_pool, const int32_t *block_table,
+                          int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                          int32_t num_seqs, int32_t chunk_len, int32_t num_q_heads,
+                          int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                          int32_t num_pages, float scale, pa_dtype dtype,
+                          int32_t *dev_err, pa_stream_t stream);
+
 /* Size of the library-owned partials array behind pa_decode_splitkv_noalloc. */
 #define PA_NOALLOC_SCRATCH_BYTES (32u << 20)
 

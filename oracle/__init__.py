@@ -16,4 +16,5 @@ from .paged_attention import (  # noqa: F401
     splitkv_partials,
     merge_partials,
     cache_append,
+    paged_decode_chunk,
 )

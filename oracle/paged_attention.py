@@ -25,6 +25,10 @@ What it follows:
 * Cache append: "grow the table, scatter the K/V" (nanoserve Day 20,
   section "What I learned"); the table is grown by the caller, the scatter
   writes each new token's K and V rows into its page slot.
+* Chunked multi-query read: nanoserve "Day 23: the real triton.jit
+  paged-attention kernel" (section "What I added today") gives every query
+  position i of a chunk its own program and a causal offset ``past``: query
+  i sits at position past + i and sees tokens 0 .. past + i.
 
 Readings where the pages are silent (each one is listed in the design notes):
 
@@ -35,6 +39,9 @@ Readings where the pages are silent (each one is listed in the design notes):
   is -inf; a split with no tokens has lse -inf and output 0.
 * A split of ``pages_per_split`` pages covers tokens
   [s * pages_per_split * page_size, min(len, (s+1) * pages_per_split * page_size)).
+* In a chunk of n_q queries, seq_len counts the history and the chunk, so
+  past = seq_len - n_q; a query whose position is negative sees nothing and
+  its output is 0.
 
 Every pin of this oracle lives in tests/test_oracle_pins.py.
 """
@@ -194,3 +201,29 @@ def cache_append(k_pool, v_pool, k_new, v_new, block_table, positions,
         k_out[page, slot] = k_new[i]
         v_out[page, slot] = v_new[i]
     return k_out, v_out
+
+
+def paged_decode_chunk(q, k_pool, v_pool, block_table, seq_lens, scale: float,
+                       page_size: int):
+    """Causal read of a chunk of queries per sequence: out [B, n_q, Hq, d] (float64).
+
+    q [B, n_q, Hq, d].  Query i of sequence b sits at position
+    past_b + i with past_b = seq_lens[b] - n_q, and attends to tokens
+    0 .. past_b + i of the sequence (read through its block table).
+    """
+    b_n, n_q, n_h, d = q.shape
+    n_kv = k_pool.shape[2]
+    out = np.zeros(q.shape, dtype=np.float64)
+    for b in range(b_n):
+        n = int(seq_lens[b])
+        past = n - n_q
+        k_hist, v_hist = gather_history(k_pool, v_pool, block_table[b], n, page_size)
+        for i in range(n_q):
+            seen = past + i + 1          # tokens 0 .. past + i
+            if seen <= 0:
+                continue
+            for h in range(n_h):
+                g = kv_head_of(h, n_h, n_kv)
+                out[b, i, h], _ = attend(q[b, i, h], k_hist[:seen, g, :], v_hist[:seen, g, :],
+                                         scale)
+    return out

@@ -7,8 +7,8 @@ CUDA stream.  All arithmetic runs in the library's CUDA kernels; there is
 no other implementation to fall back on, so a missing library raises.
 
 The names match the C ABI: pa_cache_append, pa_decode, pa_decode_splitkv,
-pa_merge, pa_decode_splitkv_noalloc, pa_num_splits, pa_status_string,
-pa_version.
+pa_merge, pa_decode_chunk, pa_decode_splitkv_noalloc, pa_num_splits,
+pa_status_string, pa_version.
 """
 
 from __future__ import annotations
@@ -26,7 +26,8 @@ PA_F32, PA_F16, PA_BF16 = 0, 1, 2
 PA_DEV_OK, PA_DEV_BAD_PAGE, PA_DEV_BAD_POSITION, PA_DEV_BAD_SEQ_LEN, PA_DEV_BAD_SEQ_ID = 0, 1, 2, 3, 4
 
 EXPORTED = ("pa_status_string", "pa_version", "pa_num_splits", "pa_cache_append",
-            "pa_decode", "pa_decode_splitkv", "pa_merge", "pa_decode_splitkv_noalloc")
+            "pa_decode", "pa_decode_splitkv", "pa_merge", "pa_decode_splitkv_noalloc",
+            "pa_decode_chunk")
 
 # bytes of the library-owned partials array behind pa_decode_splitkv_noalloc
 PA_NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -48,6 +49,8 @@ _SIGNATURES = {
     "pa_decode_splitkv": (ctypes.c_int, [_p, _p, _p, _p, _p, _p, _i, _p, _i, _i, _i, _i, _i, _i,
                                          _f, _i, _i, ctypes.c_int, _p, _p]),
     "pa_merge": (ctypes.c_int, [_p, _p, _p, _i, _i, _i, _i, ctypes.c_int, _p]),
+    "pa_decode_chunk": (ctypes.c_int, [_p, _p, _p, _p, _p, _i, _p, _i, _i, _i, _i, _i, _i, _i, _f,
+                                       ctypes.c_int, _p, _p]),
     "pa_decode_splitkv_noalloc": (ctypes.c_int, [_p, _p, _p, _p, _p, _i, _p, _i, _i, _i, _i, _i,
                                                  _i, _f, _i, ctypes.c_int, _p, _p]),
 }
@@ -189,6 +192,25 @@ def pa_decode_splitkv(partial_out, partial_lse, q, k_pool, v_pool, block_table, 
         float(scale), int(pages_per_split), max_splits, _dtype_code(q),
         _ptr(dev_err, "dev_err", torch.int32, allow_none=True), _stream(stream))
     _check("pa_decode_splitkv", st)
+
+
+def pa_decode_chunk(out, q, k_pool, v_pool, block_table, seq_lens, scale: float, dev_err=None,
+                    stream=None) -> None:
+    """Causal read of q [B, n_q, Hq, d]: query i sees tokens 0 .. seq_len - n_q + i."""
+    import torch
+    lib = load()
+    num_pages, block_size, hkv, d = k_pool.shape
+    b, nq, hq, dq = q.shape
+    if dq != d or out.shape != q.shape or v_pool.shape != k_pool.shape:
+        raise ValueError("pa_decode_chunk: inconsistent shapes")
+    dt = q.dtype
+    st = lib.pa_decode_chunk(
+        _ptr(out, "out", dt), _ptr(q, "q", dt), _ptr(k_pool, "k_pool", dt),
+        _ptr(v_pool, "v_pool", dt), _ptr(block_table, "block_table", torch.int32),
+        block_table.shape[1], _ptr(seq_lens, "seq_lens", torch.int32), b, nq, hq, hkv, d,
+        block_size, num_pages, float(scale), _dtype_code(q),
+        _ptr(dev_err, "dev_err", torch.int32, allow_none=True), _stream(stream))
+    _check("pa_decode_chunk", st)
 
 
 def pa_merge(out, partial_out, partial_lse, stream=None) -> None:

@@ -49,6 +49,18 @@ struct DecodeParams {
   float scale_log2;         // scale * log2(e): scores kept in base-2 units
 };
 
+// Arguments of the chunked multi-query read (pa_decode_chunk).
+struct ChunkParams {
+  void *out;                   // [B][chunk_len][Hq][D]
+  const void *q;               // [B][chunk_len][Hq][D]
+  const void *k_pool, *v_pool;
+  const int32_t *block_table, *seq_lens;
+  int32_t *dev_err;
+  int32_t num_seqs, chunk_len, num_q_heads, num_kv_heads, head_dim, group;
+  int32_t max_blocks, block_size_log2, num_pages;
+  float scale_log2;
+};
+
 struct AppendParams {
   const void *k_new, *v_new;  // [T][Hkv][D]
   void *k_pool, *v_pool;
@@ -70,6 +82,10 @@ cudaError_t launch_decode_simt(const DecodeParams &p, pa_dtype dtype, cudaStream
 // Tensor-core read: f16/bf16, head_dim in {32, 48, 64, 96, 128, 256}, groups of up to 16.
 bool mma_supports(pa_dtype dtype, int head_dim, int group);
 cudaError_t launch_decode_mma(const DecodeParams &p, pa_dtype dtype, cudaStream_t stream);
+// Chunked multi-query read: f16/bf16, head_dim in {32, 48, 64, 96, 128}.
+bool chunk_supports(pa_dtype dtype, int head_dim);
+int chunk_rows_per_cta();
+cudaError_t launch_chunk(const ChunkParams &p, pa_dtype dtype, cudaStream_t stream);
 cudaError_t launch_append(const AppendParams &p, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams &p, pa_dtype dtype, cudaStream_t stream);
 

@@ -178,3 +178,23 @@ def test_noalloc_validation_before_any_device_call(lib, kw, want):
         a["out"], a["q"], a["k"], a["v"], a["bt"], a["mb"], a["sl"], a["b"], a["hq"], a["hkv"],
         a["d"], a["bs"], a["np_"], a["scale"], a["pps"], a["dt"], None, None)
     assert st == want
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(nq=0), pa.PA_ERR_INVALID_ARG),
+    (dict(dt=pa.PA_F32), pa.PA_ERR_UNSUPPORTED),          # tensor-core read only
+    (dict(d=256), pa.PA_ERR_UNSUPPORTED),
+    (dict(d=80), pa.PA_ERR_UNSUPPORTED),
+    (dict(hq=9, hkv=2), pa.PA_ERR_INVALID_ARG),
+    (dict(q=MISALIGNED), pa.PA_ERR_INVALID_ARG),
+    (dict(b=0), pa.PA_OK),
+    (dict(b=0, hq=16, hkv=1, nq=4096), pa.PA_OK),
+])
+def test_chunk_validation(lib, kw, want):
+    a = dict(out=FAKE, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, mb=4, sl=FAKE, b=2, nq=8, hq=8, hkv=2,
+             d=64, bs=16, np_=32, scale=0.125, dt=pa.PA_BF16)
+    a.update(kw)
+    st = lib.raw().pa_decode_chunk(a["out"], a["q"], a["k"], a["v"], a["bt"], a["mb"], a["sl"],
+                                   a["b"], a["nq"], a["hq"], a["hkv"], a["d"], a["bs"], a["np_"],
+                                   a["scale"], a["dt"], None, None)
+    assert st == want

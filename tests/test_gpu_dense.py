@@ -21,7 +21,7 @@ def _read(lib, g, splits):
     if splits == 1:
         lib.pa_decode(out, g.q, g.k_pool, g.v_pool, g.block_table, g.seq_lens, g.scale)
         return out
-    pps = g.max_blocks // splits
+    pps = max(1, g.max_blocks // splits)  # a split is at least one 16-token page
     s = lib.pa_num_splits(g.max_blocks, pps)
     po = torch.empty((g.num_seqs, g.num_q_heads, s, g.head_dim), device="cuda")
     pl = torch.empty((g.num_seqs, g.num_q_heads, s), device="cuda")
