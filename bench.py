@@ -56,6 +56,8 @@ def parse_args():
     ap.add_argument("--history", type=int, default=4096)
     ap.add_argument("--no-extras", action="store_true",
                     help="headline step only (no sweep, long-context, ragged, CPU baseline)")
+    ap.add_argument("--only", choices=["sweep", "longctx", "ragged8b", "dense_vs_sdpa", "chunk"],
+                    help="run one extra section alone and print its JSON (for profiling)")
     return ap.parse_args()
 
 
@@ -289,6 +291,16 @@ def main():
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if args.only:
+        pa.load()
+        peak, _ = measured_peaks()
+        fns = {"sweep": lambda: sweep(pa, workloads, torch, dev, L2Flush(torch, dev), peak),
+               "longctx": lambda: longctx(pa, workloads, torch, dev, peak),
+               "ragged8b": lambda: ragged(pa, workloads, torch, dev, peak),
+               "dense_vs_sdpa": lambda: dense_vs_sdpa(pa, workloads, torch, dev, peak),
+               "chunk": lambda: chunk(pa, workloads, torch, dev, peak)}
+        print(json.dumps({args.only: fns[args.only]()}), flush=True)
+        return
     dist = None
     if world > 1:
         import torch.distributed as dist
