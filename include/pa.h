@@ -165,7 +165,8 @@ pa_status pa_decode_splitkv(float *partial_out, float *partial_lse,
  * w_s = exp(partial_lse[b][h][s] - M), and
  *   out[b][h] = sum_s w_s * partial_out[b][h][s] / sum_s w_s,
  * rounded to dtype.  A row whose splits are all empty (every lse -inf)
- * gives 0.  fp32 arithmetic.
+ * gives 0.  fp32 arithmetic.  head_dim must be a multiple of 4 (every
+ * supported read produces one) and partial_out 16-byte aligned.
  */
 pa_status pa_merge(void *out, const float *partial_out,
                    const float *partial_lse, int32_t num_seqs,

@@ -248,11 +248,12 @@ pa_status pa_merge(void *out, const float *partial_out, const float *partial_lse
   if (num_seqs < 0 || num_q_heads <= 0 || max_splits <= 0 || head_dim <= 0)
     return PA_ERR_INVALID_ARG;
   if (elem_size(dtype) == 0) return PA_ERR_INVALID_ARG;
-  if (head_dim > kMaxHeadDim) return PA_ERR_UNSUPPORTED;
+  if (head_dim > kMaxHeadDim || head_dim % 4 != 0) return PA_ERR_UNSUPPORTED;
   const int64_t rows = static_cast<int64_t>(num_seqs) * num_q_heads;
   if (rows > INT32_MAX / 4) return PA_ERR_UNSUPPORTED;
   if (rows == 0) return PA_OK;
   if (!out || !partial_out || !partial_lse) return PA_ERR_INVALID_ARG;
+  if (!aligned16(partial_out)) return PA_ERR_INVALID_ARG;  // read as float4 rows
   pa::MergeParams p{};
   p.out = out;
   p.partial_out = partial_out;

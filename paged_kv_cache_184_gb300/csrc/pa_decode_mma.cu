@@ -18,7 +18,11 @@
 //
 // Every warp owns every NW-th tile of the CTA's token range and streams it
 // through its own NS-stage cp.async ring (no CTA barrier in the main loop);
-// the warps' (m, l, O) states are combined once at the end.  Rows are stored
+// the warps' (m, l, O) states are combined at the end of every split.  In
+// the split read a CTA may cover several consecutive splits of one
+// (sequence, kv head): the warps' copies run on across split boundaries
+// while each finished split is combined in a separate area, so one
+// pipeline ramp serves all of them and the whole grid fits one wave.  Rows are stored
 // with a 16-byte-chunk XOR swizzle so that ldmatrix is bank-conflict free.
 // Tokens past the end of the range are zero-filled by the copy and masked
 // to -inf in the scores.
@@ -123,7 +127,7 @@ __global__ void __launch_bounds__(kThreads)
   using S = Shape<D, NT>;
   using M = MmaT<T>;
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ int s_bad;
+  __shared__ unsigned s_bad;  // bit s: split s of this CTA met a bad page
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -133,13 +137,15 @@ __global__ void __launch_bounds__(kThreads)
 
   const int hkv = p.num_kv_heads;
   const int g = blockIdx.x % hkv;
-  const int split = blockIdx.x / hkv;
+  const int s0 = (blockIdx.x / hkv) * p.splits_per_cta;  // first split of this CTA
+  const int nsplit = min(p.splits_per_cta, p.num_splits - s0);
   const int b = blockIdx.y;
   const int G = p.group;
   const int bs_log2 = p.block_size_log2;
   const int bs_mask = (1 << bs_log2) - 1;
+  const bool multi = p.splits_per_cta > 1;
 
-  if (tid == 0) s_bad = 0;
+  if (tid == 0) s_bad = 0u;
   pdl_wait();
 
   // The prologue issues its independent loads together: the length, q, and
@@ -149,7 +155,7 @@ __global__ void __launch_bounds__(kThreads)
   const long long cap = static_cast<long long>(p.max_blocks) << bs_log2;
   const long long span =
       p.pages_per_split > 0 ? static_cast<long long>(p.pages_per_split) << bs_log2 : cap;
-  const long long lo = p.pages_per_split > 0 ? static_cast<long long>(split) * span : 0;
+  const long long lo = p.pages_per_split > 0 ? static_cast<long long>(s0) * span : 0;
   int pid_pre[S::kStages];
 #pragma unroll
   for (int s = 0; s < S::kStages; ++s) {
@@ -187,7 +193,9 @@ __global__ void __launch_bounds__(kThreads)
     len = 0;
   }
   const int t_begin = static_cast<int>(min(static_cast<long long>(len), lo));
-  const int t_end = static_cast<int>(min(static_cast<long long>(len), lo + span));
+  const int t_end = static_cast<int>(min(static_cast<long long>(len), lo + nsplit * span));
+  // tiles per split (a CTA covers several splits only when a split is whole tiles)
+  const int tiles_per_split = multi ? static_cast<int>(span / kTile) : 0x7fffffff;
 
   const T *kpool = static_cast<const T *>(p.k_pool);
   const T *vpool = static_cast<const T *>(p.v_pool);
@@ -226,7 +234,7 @@ __global__ void __launch_bounds__(kThreads)
       if (valid) {
         if (page < 0 || page >= p.num_pages) {
           report_error(p.dev_err, PA_DEV_BAD_PAGE);
-          s_bad = 1;
+          atomicOr(&s_bad, 1u << static_cast<int>((pos - lo) / span));
           valid = false;
         } else {
           const size_t prow = (static_cast<size_t>(page) << bs_log2) + (pos & bs_mask);
@@ -262,7 +270,91 @@ __global__ void __launch_bounds__(kThreads)
   }
   const float sl2 = p.scale_log2;
 
+  // Combine the warps' states of relative split `srel` and write its output
+  // (or partial and lse).  Every warp calls this once per split of the CTA,
+  // in order, so the barriers inside always match.
+  const int ch = p.comb_heads;
+  auto finalize = [&](int srel) {
+    // per-lane partial sums of l cover tokens r, r+8 only: finish them
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        l[nt][0] += __shfl_xor_sync(0xffffffffu, l[nt][0], off);
+        l[nt][1] += __shfl_xor_sync(0xffffffffu, l[nt][1], off);
+      }
+    // one split per CTA: the combine reuses the ring once every warp is done
+    // with it; several: it has its own area past the ring, which keeps filling
+    float *sm_m = reinterpret_cast<float *>(multi ? smem + S::kRingBytes : smem);
+    float *sm_l = sm_m + kWarps * ch;  // [warp][head]
+    float *sm_o = sm_l + kWarps * ch;  // [warp][head][D]
+    if (!multi) __syncthreads();
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int h0 = nt * 8 + 2 * c;
+      if (h0 < ch) {
+        if (r == 0) {
+          sm_m[warp * ch + h0] = m[nt][0];
+          sm_m[warp * ch + h0 + 1] = m[nt][1];
+          sm_l[warp * ch + h0] = l[nt][0];
+          sm_l[warp * ch + h0 + 1] = l[nt][1];
+        }
+#pragma unroll
+        for (int mt = 0; mt < S::kSteps; ++mt) {
+          const int d0 = mt * 16 + r;
+          float *ob = sm_o + (warp * ch + h0) * D;
+          ob[d0] = o[mt][nt][0];
+          ob[D + d0] = o[mt][nt][1];
+          ob[d0 + 8] = o[mt][nt][2];
+          ob[D + d0 + 8] = o[mt][nt][3];
+        }
+      }
+    }
+    __syncthreads();
+    const bool bad = bad_len || ((s_bad >> srel) & 1u);
+    const bool is_split = p.pages_per_split > 0;
+    for (int idx = tid; idx < G * D; idx += kThreads) {
+      const int h = idx / D;
+      const int d = idx - h * D;
+      float Mx = -CUDART_INF_F;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) Mx = fmaxf(Mx, sm_m[w * ch + h]);
+      float L = 0.f, O = 0.f;
+      if (Mx != -CUDART_INF_F) {
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          const float wgt = exp2f(sm_m[w * ch + h] - Mx);
+          L = fmaf(sm_l[w * ch + h], wgt, L);
+          O = fmaf(sm_o[(w * ch + h) * D + d], wgt, O);
+        }
+      }
+      const bool empty = bad || (Mx == -CUDART_INF_F);
+      const float res = empty ? 0.f : O / L;
+      const size_t qh = static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(g) * G + h;
+      if (is_split) {
+        const size_t row = qh * p.num_splits + s0 + srel;
+        p.partial_out[row * D + d] = res;
+        if (d == 0)
+          p.partial_lse[row] = empty ? -CUDART_INF_F : (Mx + log2f(L)) * 0.69314718055994531f;
+      } else {
+        static_cast<T *>(p.out)[qh * D + d] = cvt_out<T>(res);
+      }
+    }
+    __syncthreads();  // the combine area is free for the next split
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      m[nt][0] = m[nt][1] = -CUDART_INF_F;
+      l[nt][0] = l[nt][1] = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < S::kSteps; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[mt][nt][e] = 0.f;
+    }
+  };
+
+  int cur = 0;  // relative split the warp is accumulating
   for (int i = 0; i < my_tiles; ++i) {
+    while (cur < (warp + i * kWarps) / tiles_per_split) finalize(cur++);
     cp_async_wait<S::kStages - 2>();
     __syncwarp();
     {
@@ -350,81 +442,47 @@ __global__ void __launch_bounds__(kThreads)
   }
   cp_async_wait_all();
   pdl_trigger();  // the merge (or the next read) may start launching
-
-  // per-lane partial sums of l cover tokens r, r+8 only: finish them
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      l[nt][0] += __shfl_xor_sync(0xffffffffu, l[nt][0], off);
-      l[nt][1] += __shfl_xor_sync(0xffffffffu, l[nt][1], off);
-    }
-  __syncthreads();  // every warp done with its ring: reuse smem for the combine
-
-  float *sm_m = reinterpret_cast<float *>(smem);          // [warp][head]
-  float *sm_l = sm_m + kWarps * S::kHeads;                 // [warp][head]
-  float *sm_o = sm_l + kWarps * S::kHeads;                 // [warp][head][D]
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int h0 = nt * 8 + 2 * c;
-    if (r == 0) {
-      sm_m[warp * S::kHeads + h0] = m[nt][0];
-      sm_m[warp * S::kHeads + h0 + 1] = m[nt][1];
-      sm_l[warp * S::kHeads + h0] = l[nt][0];
-      sm_l[warp * S::kHeads + h0 + 1] = l[nt][1];
-    }
-#pragma unroll
-    for (int mt = 0; mt < S::kSteps; ++mt) {
-      const int d0 = mt * 16 + r;
-      float *ob = sm_o + (warp * S::kHeads + h0) * D;
-      ob[d0] = o[mt][nt][0];
-      ob[D + d0] = o[mt][nt][1];
-      ob[d0 + 8] = o[mt][nt][2];
-      ob[D + d0 + 8] = o[mt][nt][3];
-    }
-  }
-  __syncthreads();
-
-  const bool bad = bad_len || (s_bad != 0);
-  const bool is_split = p.pages_per_split > 0;
-  for (int idx = tid; idx < G * D; idx += kThreads) {
-    const int h = idx / D;
-    const int d = idx - h * D;
-    float Mx = -CUDART_INF_F;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) Mx = fmaxf(Mx, sm_m[w * S::kHeads + h]);
-    float L = 0.f, O = 0.f;
-    if (Mx != -CUDART_INF_F) {
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float wgt = exp2f(sm_m[w * S::kHeads + h] - Mx);
-        L = fmaf(sm_l[w * S::kHeads + h], wgt, L);
-        O = fmaf(sm_o[(w * S::kHeads + h) * D + d], wgt, O);
-      }
-    }
-    const bool empty = bad || (Mx == -CUDART_INF_F);
-    const float res = empty ? 0.f : O / L;
-    const size_t qh = static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(g) * G + h;
-    if (is_split) {
-      const size_t row = qh * p.num_splits + split;
-      p.partial_out[row * D + d] = res;
-      if (d == 0)
-        p.partial_lse[row] = empty ? -CUDART_INF_F : (Mx + log2f(L)) * 0.69314718055994531f;
-    } else {
-      static_cast<T *>(p.out)[qh * D + d] = cvt_out<T>(res);
-    }
-  }
+  while (cur < nsplit) finalize(cur++);
 }
 
 template <typename T, int D, int NT>
-cudaError_t launch_shape(const DecodeParams &p, cudaStream_t stream) {
+cudaError_t launch_shape(DecodeParams p, cudaStream_t stream) {
   using S = Shape<D, NT>;
   auto kern = decode_mma_kernel<T, D, NT>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         S::kSmemBytes);
+  p.splits_per_cta = 1;
+  p.comb_heads = S::kHeads;
+  int smem = S::kSmemBytes;
+  if (p.pages_per_split > 0 && ((p.pages_per_split << p.block_size_log2) % kTile) == 0) {
+    // Several splits per CTA when one wave cannot hold a CTA per split but
+    // can hold one per (sequence, kv head): the fewest splits per CTA that
+    // make the grid fit the resident slots.
+    const int ch = p.group <= 4 ? 4 : S::kHeads;
+    const int smem_multi = S::kRingBytes + kWarps * ch * (D + 2) * 4;
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_multi);
+    if (err == cudaSuccess)
+      err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem_multi);
+    if (err != cudaSuccess) return err;
+    const long long pairs = static_cast<long long>(p.num_seqs) * p.num_kv_heads;
+    const long long slots = static_cast<long long>(sms) * per_sm;
+    if (pairs * p.num_splits > slots && pairs <= slots) {
+      const long long groups = slots / pairs;  // CTAs per (sequence, kv head)
+      const int k = static_cast<int>((p.num_splits + groups - 1) / groups);
+      if (k > 1 && k <= 32) {
+        p.splits_per_cta = k;
+        p.comb_heads = ch;
+        smem = smem_multi;
+      }
+    }
+  }
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  dim3 grid(p.num_splits * p.num_kv_heads, p.num_seqs);
-  return launch_pdl(kern, grid, dim3(kThreads), S::kSmemBytes, stream, p);
+  const int groups = (p.num_splits + p.splits_per_cta - 1) / p.splits_per_cta;
+  dim3 grid(groups * p.num_kv_heads, p.num_seqs);
+  return launch_pdl(kern, grid, dim3(kThreads), smem, stream, p);
 }
 
 template <typename T, int D>

@@ -45,7 +45,9 @@ struct DecodeParams {
   int32_t num_seqs, num_q_heads, num_kv_heads, head_dim, group;
   int32_t max_blocks, block_size_log2, num_pages;
   int32_t pages_per_split;  // 0: one split spanning the whole sequence
-  int32_t num_splits;       // grid splits per sequence (1 when pages_per_split == 0)
+  int32_t num_splits;       // splits per sequence, the partials' split stride (1 if unsplit)
+  int32_t splits_per_cta;   // consecutive splits one CTA reads (tensor-core read; else 1)
+  int32_t comb_heads;       // head slots per warp in the combine area (tensor-core read)
   float scale_log2;         // scale * log2(e): scores kept in base-2 units
 };
 

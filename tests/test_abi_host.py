@@ -118,6 +118,8 @@ def test_splitkv_validation(lib, kw, want):
     ((FAKE, FAKE, FAKE, 2, 4, 3, 64, 5), pa.PA_ERR_INVALID_ARG),
     ((None, FAKE, FAKE, 2, 4, 3, 64, pa.PA_BF16), pa.PA_ERR_INVALID_ARG),
     ((FAKE, FAKE, FAKE, 0, 4, 3, 64, pa.PA_BF16), pa.PA_OK),
+    ((FAKE, FAKE, FAKE, 2, 4, 3, 6, pa.PA_F32), pa.PA_ERR_UNSUPPORTED),    # not float4 rows
+    ((FAKE, MISALIGNED, FAKE, 2, 4, 3, 64, pa.PA_BF16), pa.PA_ERR_INVALID_ARG),
 ])
 def test_merge_validation(lib, args, want):
     assert lib.raw().pa_merge(*args, None) == want
