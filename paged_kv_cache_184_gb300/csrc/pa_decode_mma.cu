@@ -121,7 +121,7 @@ __device__ __forceinline__ uint32_t tile_off(int row, int chunk) {
   return row * Shape<D, NT>::kPitch + ((chunk ^ (row & 7)) << 4);
 }
 
-template <typename T, int D, int NT>
+template <typename T, int D, int NT, bool MULTI>
 __global__ void __launch_bounds__(kThreads)
     decode_mma_kernel(const DecodeParams p) {
   using S = Shape<D, NT>;
@@ -143,7 +143,6 @@ __global__ void __launch_bounds__(kThreads)
   const int G = p.group;
   const int bs_log2 = p.block_size_log2;
   const int bs_mask = (1 << bs_log2) - 1;
-  const bool multi = p.splits_per_cta > 1;
 
   if (tid == 0) s_bad = 0u;
   pdl_wait();
@@ -195,7 +194,7 @@ __global__ void __launch_bounds__(kThreads)
   const int t_begin = static_cast<int>(min(static_cast<long long>(len), lo));
   const int t_end = static_cast<int>(min(static_cast<long long>(len), lo + nsplit * span));
   // tiles per split (a CTA covers several splits only when a split is whole tiles)
-  const int tiles_per_split = multi ? static_cast<int>(span / kTile) : 0x7fffffff;
+  const int tiles_per_split = MULTI ? static_cast<int>(span / kTile) : 0x7fffffff;
 
   const T *kpool = static_cast<const T *>(p.k_pool);
   const T *vpool = static_cast<const T *>(p.v_pool);
@@ -234,7 +233,8 @@ __global__ void __launch_bounds__(kThreads)
       if (valid) {
         if (page < 0 || page >= p.num_pages) {
           report_error(p.dev_err, PA_DEV_BAD_PAGE);
-          atomicOr(&s_bad, 1u << static_cast<int>((pos - lo) / span));
+          // the tile lies inside one split: (its index in the CTA) / tiles per split
+          atomicOr(&s_bad, MULTI ? 1u << ((warp + i * kWarps) / tiles_per_split) : 1u);
           valid = false;
         } else {
           const size_t prow = (static_cast<size_t>(page) << bs_log2) + (pos & bs_mask);
@@ -270,9 +270,9 @@ __global__ void __launch_bounds__(kThreads)
   }
   const float sl2 = p.scale_log2;
 
-  // Combine the warps' states of relative split `srel` and write its output
-  // (or partial and lse).  Every warp calls this once per split of the CTA,
-  // in order, so the barriers inside always match.
+  // Several splits per CTA: combine the warps' states of relative split
+  // `srel` and write its partial and lse.  Every warp calls this once per
+  // split of the CTA, in order, so the barriers inside always match.
   const int ch = p.comb_heads;
   auto finalize = [&](int srel) {
     // per-lane partial sums of l cover tokens r, r+8 only: finish them
@@ -283,12 +283,10 @@ __global__ void __launch_bounds__(kThreads)
         l[nt][0] += __shfl_xor_sync(0xffffffffu, l[nt][0], off);
         l[nt][1] += __shfl_xor_sync(0xffffffffu, l[nt][1], off);
       }
-    // one split per CTA: the combine reuses the ring once every warp is done
-    // with it; several: it has its own area past the ring, which keeps filling
-    float *sm_m = reinterpret_cast<float *>(multi ? smem + S::kRingBytes : smem);
+    // the combine area lies past the ring, which keeps filling meanwhile
+    float *sm_m = reinterpret_cast<float *>(smem + S::kRingBytes);
     float *sm_l = sm_m + kWarps * ch;  // [warp][head]
     float *sm_o = sm_l + kWarps * ch;  // [warp][head][D]
-    if (!multi) __syncthreads();
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int h0 = nt * 8 + 2 * c;
@@ -354,7 +352,9 @@ __global__ void __launch_bounds__(kThreads)
 
   int cur = 0;  // relative split the warp is accumulating
   for (int i = 0; i < my_tiles; ++i) {
-    while (cur < (warp + i * kWarps) / tiles_per_split) finalize(cur++);
+    if constexpr (MULTI) {
+      while (cur < (warp + i * kWarps) / tiles_per_split) finalize(cur++);
+    }
     cp_async_wait<S::kStages - 2>();
     __syncwarp();
     {
@@ -442,13 +442,82 @@ __global__ void __launch_bounds__(kThreads)
   }
   cp_async_wait_all();
   pdl_trigger();  // the merge (or the next read) may start launching
-  while (cur < nsplit) finalize(cur++);
+  if constexpr (MULTI) {
+    while (cur < nsplit) finalize(cur++);
+  } else {
+
+    // One split per CTA: combine once, reusing the ring.
+    // per-lane partial sums of l cover tokens r, r+8 only: finish them
+  #pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+  #pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        l[nt][0] += __shfl_xor_sync(0xffffffffu, l[nt][0], off);
+        l[nt][1] += __shfl_xor_sync(0xffffffffu, l[nt][1], off);
+      }
+    __syncthreads();  // every warp done with its ring: reuse smem for the combine
+
+    float *sm_m = reinterpret_cast<float *>(smem);  // [warp][head]
+    float *sm_l = sm_m + kWarps * S::kHeads;         // [warp][head]
+    float *sm_o = sm_l + kWarps * S::kHeads;         // [warp][head][D]
+  #pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int h0 = nt * 8 + 2 * c;
+      if (r == 0) {
+        sm_m[warp * S::kHeads + h0] = m[nt][0];
+        sm_m[warp * S::kHeads + h0 + 1] = m[nt][1];
+        sm_l[warp * S::kHeads + h0] = l[nt][0];
+        sm_l[warp * S::kHeads + h0 + 1] = l[nt][1];
+      }
+  #pragma unroll
+      for (int mt = 0; mt < S::kSteps; ++mt) {
+        const int d0 = mt * 16 + r;
+        float *ob = sm_o + (warp * S::kHeads + h0) * D;
+        ob[d0] = o[mt][nt][0];
+        ob[D + d0] = o[mt][nt][1];
+        ob[d0 + 8] = o[mt][nt][2];
+        ob[D + d0 + 8] = o[mt][nt][3];
+      }
+    }
+    __syncthreads();
+
+    const bool bad = bad_len || (s_bad != 0u);
+    const bool is_split = p.pages_per_split > 0;
+    for (int idx = tid; idx < G * D; idx += kThreads) {
+      const int h = idx / D;
+      const int d = idx - h * D;
+      float Mx = -CUDART_INF_F;
+  #pragma unroll
+      for (int w = 0; w < kWarps; ++w) Mx = fmaxf(Mx, sm_m[w * S::kHeads + h]);
+      float L = 0.f, O = 0.f;
+      if (Mx != -CUDART_INF_F) {
+  #pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          const float wgt = exp2f(sm_m[w * S::kHeads + h] - Mx);
+          L = fmaf(sm_l[w * S::kHeads + h], wgt, L);
+          O = fmaf(sm_o[(w * S::kHeads + h) * D + d], wgt, O);
+        }
+      }
+      const bool empty = bad || (Mx == -CUDART_INF_F);
+      const float res = empty ? 0.f : O / L;
+      const size_t qh = static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(g) * G + h;
+      if (is_split) {
+        const size_t row = qh * p.num_splits + s0;
+        p.partial_out[row * D + d] = res;
+        if (d == 0)
+          p.partial_lse[row] = empty ? -CUDART_INF_F : (Mx + log2f(L)) * 0.69314718055994531f;
+      } else {
+        static_cast<T *>(p.out)[qh * D + d] = cvt_out<T>(res);
+      }
+    }
+  }
 }
 
 template <typename T, int D, int NT>
 cudaError_t launch_shape(DecodeParams p, cudaStream_t stream) {
   using S = Shape<D, NT>;
-  auto kern = decode_mma_kernel<T, D, NT>;
+  auto kern = decode_mma_kernel<T, D, NT, false>;
+  auto kern_multi = decode_mma_kernel<T, D, NT, true>;
   p.splits_per_cta = 1;
   p.comb_heads = S::kHeads;
   int smem = S::kSmemBytes;
@@ -462,9 +531,11 @@ cudaError_t launch_shape(DecodeParams p, cudaStream_t stream) {
     cudaError_t err = cudaGetDevice(&dev);
     if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (err == cudaSuccess)
-      err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_multi);
+      err = cudaFuncSetAttribute(kern_multi, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 smem_multi);
     if (err == cudaSuccess)
-      err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem_multi);
+      err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern_multi, kThreads,
+                                                          smem_multi);
     if (err != cudaSuccess) return err;
     const long long pairs = static_cast<long long>(p.num_seqs) * p.num_kv_heads;
     const long long slots = static_cast<long long>(sms) * per_sm;
@@ -478,10 +549,11 @@ cudaError_t launch_shape(DecodeParams p, cudaStream_t stream) {
       }
     }
   }
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (err != cudaSuccess) return err;
   const int groups = (p.num_splits + p.splits_per_cta - 1) / p.splits_per_cta;
   dim3 grid(groups * p.num_kv_heads, p.num_seqs);
+  if (p.splits_per_cta > 1) return launch_pdl(kern_multi, grid, dim3(kThreads), smem, stream, p);
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
   return launch_pdl(kern, grid, dim3(kThreads), smem, stream, p);
 }
 
