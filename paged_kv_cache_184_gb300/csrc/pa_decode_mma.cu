@@ -445,12 +445,11 @@ __global__ void __launch_bounds__(kThreads)
   if constexpr (MULTI) {
     while (cur < nsplit) finalize(cur++);
   } else {
-
     // One split per CTA: combine once, reusing the ring.
     // per-lane partial sums of l cover tokens r, r+8 only: finish them
-  #pragma unroll
+#pragma unroll
     for (int nt = 0; nt < NT; ++nt)
-  #pragma unroll
+#pragma unroll
       for (int off = 4; off < 32; off <<= 1) {
         l[nt][0] += __shfl_xor_sync(0xffffffffu, l[nt][0], off);
         l[nt][1] += __shfl_xor_sync(0xffffffffu, l[nt][1], off);
@@ -460,7 +459,7 @@ __global__ void __launch_bounds__(kThreads)
     float *sm_m = reinterpret_cast<float *>(smem);  // [warp][head]
     float *sm_l = sm_m + kWarps * S::kHeads;         // [warp][head]
     float *sm_o = sm_l + kWarps * S::kHeads;         // [warp][head][D]
-  #pragma unroll
+#pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int h0 = nt * 8 + 2 * c;
       if (r == 0) {
@@ -469,7 +468,7 @@ __global__ void __launch_bounds__(kThreads)
         sm_l[warp * S::kHeads + h0] = l[nt][0];
         sm_l[warp * S::kHeads + h0 + 1] = l[nt][1];
       }
-  #pragma unroll
+#pragma unroll
       for (int mt = 0; mt < S::kSteps; ++mt) {
         const int d0 = mt * 16 + r;
         float *ob = sm_o + (warp * S::kHeads + h0) * D;
@@ -487,11 +486,11 @@ __global__ void __launch_bounds__(kThreads)
       const int h = idx / D;
       const int d = idx - h * D;
       float Mx = -CUDART_INF_F;
-  #pragma unroll
+#pragma unroll
       for (int w = 0; w < kWarps; ++w) Mx = fmaxf(Mx, sm_m[w * S::kHeads + h]);
       float L = 0.f, O = 0.f;
       if (Mx != -CUDART_INF_F) {
-  #pragma unroll
+#pragma unroll
         for (int w = 0; w < kWarps; ++w) {
           const float wgt = exp2f(sm_m[w * S::kHeads + h] - Mx);
           L = fmaf(sm_l[w * S::kHeads + h], wgt, L);
