@@ -554,7 +554,31 @@ def ragged(pa, workloads, torch, dev, peak):
            "us_single_pass": 1e3 * med1, "gbs_single_pass": rb / (med1 * 1e-3) / 1e9,
            "us_split64_plus_merge": 1e3 * med2,
            "gbs_split64": (rb + split_bytes(g.num_seqs, 32, s, 128)) / (med2 * 1e-3) / 1e9}
-    res["frac_best"] = max(res["gbs_single_pass"], res["gbs_split64"]) / peak
+    # planned work lists (host plan from the lengths; items copied to the device)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    host_lens = g.seq_lens.cpu()
+    planned = []
+    for mult in (3, 6, 12, 24):
+        t0 = time.perf_counter()
+        items, slots = pa.pa_plan_work(host_lens, 8, 16, sms * mult, 16)
+        plan_us = 1e6 * (time.perf_counter() - t0)
+        d_items = items.to(dev)
+        po_w = torch.empty((g.num_seqs, 32, slots, 128), device=dev)
+        pl_w = torch.empty((g.num_seqs, 32, slots), device=dev)
+
+        def work(d_items=d_items, po_w=po_w, pl_w=pl_w):
+            pa.pa_decode_work(po_w, pl_w, d_items, g.q, g.k_pool, g.v_pool, g.block_table,
+                              g.seq_lens, g.scale)
+            pa.pa_merge(out, po_w, pl_w)
+
+        med3, _ = _time_launches(work, torch, flush, iters=10)
+        planned.append({"target_ctas": sms * mult, "items": len(items), "max_slots": slots,
+                        "us": 1e3 * med3, "plan_host_us": plan_us,
+                        "gbs": (rb + split_bytes(g.num_seqs, 32, slots, 128)) / (med3 * 1e-3) / 1e9})
+        del po_w, pl_w, d_items
+    res["planned"] = planned
+    res["frac_best"] = max([res["gbs_single_pass"], res["gbs_split64"]] +
+                           [x["gbs"] for x in planned]) / peak
     del g, out, po, pl
     torch.cuda.empty_cache()
     return res

@@ -70,7 +70,8 @@ enum {
   PA_DEV_BAD_PAGE = 1,     /* block-table entry outside [0, num_pages) */
   PA_DEV_BAD_POSITION = 2, /* append position outside [0, max_blocks_per_seq * block_size) */
   PA_DEV_BAD_SEQ_LEN = 3,  /* seq_len outside [0, max_blocks_per_seq * block_size] */
-  PA_DEV_BAD_SEQ_ID = 4    /* append seq id outside [0, num_seqs) */
+  PA_DEV_BAD_SEQ_ID = 4,   /* append seq id outside [0, num_seqs) */
+  PA_DEV_BAD_ITEM = 5      /* work item with a bad sequence, range or slot */
 };
 
 /* Human-readable name of a status code (static string). */
@@ -172,6 +173,52 @@ pa_status pa_merge(void *out, const float *partial_out,
                    const float *partial_lse, int32_t num_seqs,
                    int32_t num_q_heads, int32_t max_splits, int32_t head_dim,
                    pa_dtype dtype, pa_stream_t stream);
+
+/*
+ * pa_plan_work - host-side work plan for a ragged batch (no device access).
+ *
+ * "Three Attention Kernels" ("Key Tradeoffs") finds that more splits is not
+ * monotonically better, and the explainer page on kernels (FlashInfer,
+ * "Technical Details") plans ragged batches on the host every step.  Given
+ * the host copy of the lengths, this cuts every sequence into near-equal
+ * token ranges ("items") of at least min_pages_per_item pages, sized so
+ * that items * num_kv_heads is about target_ctas (a multiple of the SM
+ * count is a good target).  A sequence shorter than one item is one item;
+ * a sequence of length 0 is one empty item.  Items are ordered longest
+ * first.  Each item is four int32: sequence, first token, end token
+ * (exclusive), and slot | (items of that sequence << 16), slot being the
+ * item's index within its sequence.  Writes at most max_items items to
+ * `items` (host memory, [max_items][4]) and the largest per-sequence item
+ * count to *max_slots.  Returns the number of items, or -1 for bad
+ * arguments or too small a buffer (num_seqs + total pages / min pages
+ * always suffices).
+ */
+int32_t pa_plan_work(const int32_t *seq_lens, int32_t num_seqs, int32_t num_kv_heads,
+                     int32_t block_size, int32_t target_ctas, int32_t min_pages_per_item,
+                     int32_t *items, int32_t max_items, int32_t *max_slots);
+
+/*
+ * pa_decode_work - the split read over a planned work list.
+ *
+ * Runs one CTA per (item, kv head) of `items` (device memory, the
+ * [num_items][4] records of pa_plan_work, 16-byte aligned) and writes, for
+ * every item of sequence b with slot j, partial_out[b][h][j] and
+ * partial_lse[b][h][j] exactly as pa_decode_splitkv writes a split.  The
+ * last item of a sequence also sets partial_lse to -inf for its unused
+ * slots (up to max_slots; their partial_out is left as it is).  pa_merge
+ * with max_splits = max_slots then gives the output.  Every sequence must
+ * have its slots 0 .. count-1 covered exactly once, as pa_plan_work
+ * produces; a malformed item records PA_DEV_BAD_ITEM and its CTA writes
+ * nothing.  f16/bf16 with the tensor-core head dims only.
+ */
+pa_status pa_decode_work(float *partial_out, float *partial_lse, const int32_t *items,
+                         int32_t num_items, int32_t max_slots, const void *q,
+                         const void *k_pool, const void *v_pool,
+                         const int32_t *block_table, int32_t max_blocks_per_seq,
+                         const int32_t *seq_lens, int32_t num_seqs, int32_t num_q_heads,
+                         int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                         int32_t num_pages, float scale, pa_dtype dtype, int32_t *dev_err,
+                         pa_stream_t stream);
 
 /*
  * pa_decode_chunk - causal read of a chunk of queries per sequence.

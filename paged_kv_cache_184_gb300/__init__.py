@@ -7,8 +7,8 @@ CUDA stream.  All arithmetic runs in the library's CUDA kernels; there is
 no other implementation to fall back on, so a missing library raises.
 
 The names match the C ABI: pa_cache_append, pa_decode, pa_decode_splitkv,
-pa_merge, pa_decode_chunk, pa_decode_splitkv_noalloc, pa_num_splits,
-pa_status_string, pa_version.
+pa_merge, pa_decode_chunk, pa_plan_work, pa_decode_work,
+pa_decode_splitkv_noalloc, pa_num_splits, pa_status_string, pa_version.
 """
 
 from __future__ import annotations
@@ -24,10 +24,11 @@ LIB_PATH = _build.LIB_PATH
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA = 0, 1, 2, 3
 PA_F32, PA_F16, PA_BF16 = 0, 1, 2
 PA_DEV_OK, PA_DEV_BAD_PAGE, PA_DEV_BAD_POSITION, PA_DEV_BAD_SEQ_LEN, PA_DEV_BAD_SEQ_ID = 0, 1, 2, 3, 4
+PA_DEV_BAD_ITEM = 5
 
 EXPORTED = ("pa_status_string", "pa_version", "pa_num_splits", "pa_cache_append",
             "pa_decode", "pa_decode_splitkv", "pa_merge", "pa_decode_splitkv_noalloc",
-            "pa_decode_chunk")
+            "pa_decode_chunk", "pa_plan_work", "pa_decode_work")
 
 # bytes of the library-owned partials array behind pa_decode_splitkv_noalloc
 PA_NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -49,6 +50,9 @@ _SIGNATURES = {
     "pa_decode_splitkv": (ctypes.c_int, [_p, _p, _p, _p, _p, _p, _i, _p, _i, _i, _i, _i, _i, _i,
                                          _f, _i, _i, ctypes.c_int, _p, _p]),
     "pa_merge": (ctypes.c_int, [_p, _p, _p, _i, _i, _i, _i, ctypes.c_int, _p]),
+    "pa_plan_work": (_i, [_p, _i, _i, _i, _i, _i, _p, _i, _p]),
+    "pa_decode_work": (ctypes.c_int, [_p, _p, _p, _i, _i, _p, _p, _p, _p, _i, _p, _i, _i, _i, _i, _i,
+                                      _i, _f, ctypes.c_int, _p, _p]),
     "pa_decode_chunk": (ctypes.c_int, [_p, _p, _p, _p, _p, _i, _p, _i, _i, _i, _i, _i, _i, _i, _f,
                                        ctypes.c_int, _p, _p]),
     "pa_decode_splitkv_noalloc": (ctypes.c_int, [_p, _p, _p, _p, _p, _i, _p, _i, _i, _i, _i, _i,
@@ -211,6 +215,52 @@ def pa_decode_chunk(out, q, k_pool, v_pool, block_table, seq_lens, scale: float,
         block_size, num_pages, float(scale), _dtype_code(q),
         _ptr(dev_err, "dev_err", torch.int32, allow_none=True), _stream(stream))
     _check("pa_decode_chunk", st)
+
+
+def pa_plan_work(seq_lens, num_kv_heads: int, block_size: int, target_ctas: int,
+                 min_pages_per_item: int = 16):
+    """Host work plan of a ragged batch: (items int32 [n, 4] on the CPU, max_slots).
+
+    seq_lens is the host copy of the lengths (a CPU tensor or a sequence).
+    """
+    import torch
+    lib = load()
+    lens = torch.as_tensor(seq_lens, dtype=torch.int32).contiguous()
+    if lens.is_cuda:
+        raise ValueError("pa_plan_work plans from the host copy of the lengths")
+    pages = int(((lens.to(torch.int64) + block_size - 1) // block_size).sum())
+    cap = lens.numel() + pages // max(1, min_pages_per_item) + 1
+    items = torch.empty((cap, 4), dtype=torch.int32)
+    slots = ctypes.c_int32(0)
+    n = lib.pa_plan_work(lens.data_ptr(), lens.numel(), num_kv_heads, block_size, target_ctas,
+                         min_pages_per_item, items.data_ptr(), cap, ctypes.byref(slots))
+    if n < 0:
+        raise PaError("pa_plan_work", PA_ERR_INVALID_ARG)
+    return items[:n].clone(), int(slots.value)
+
+
+def pa_decode_work(partial_out, partial_lse, items, q, k_pool, v_pool, block_table, seq_lens,
+                   scale: float, dev_err=None, stream=None) -> None:
+    """Split read over a planned work list (items: device int32 [n, 4] from pa_plan_work)."""
+    import torch
+    lib = load()
+    num_pages, block_size, hkv, d = k_pool.shape
+    b, hq, _ = q.shape
+    max_slots = partial_lse.shape[2]
+    if partial_out.shape != (b, hq, max_slots, d) or partial_lse.shape != (b, hq, max_slots):
+        raise ValueError("pa_decode_work: partial shapes must be [B,Hq,S,d] and [B,Hq,S]")
+    if items.dim() != 2 or items.shape[1] != 4:
+        raise ValueError("pa_decode_work: items must be [n, 4]")
+    dt = q.dtype
+    st = lib.pa_decode_work(
+        _ptr(partial_out, "partial_out", torch.float32),
+        _ptr(partial_lse, "partial_lse", torch.float32), _ptr(items, "items", torch.int32),
+        items.shape[0], max_slots, _ptr(q, "q", dt), _ptr(k_pool, "k_pool", dt),
+        _ptr(v_pool, "v_pool", dt), _ptr(block_table, "block_table", torch.int32),
+        block_table.shape[1], _ptr(seq_lens, "seq_lens", torch.int32), b, hq, hkv, d, block_size,
+        num_pages, float(scale), _dtype_code(q),
+        _ptr(dev_err, "dev_err", torch.int32, allow_none=True), _stream(stream))
+    _check("pa_decode_work", st)
 
 
 def pa_merge(out, partial_out, partial_lse, stream=None) -> None:

@@ -203,6 +203,39 @@ pa_status pa_decode_splitkv(float *partial_out, float *partial_lse, const void *
   return launched(launch_read(p, dtype, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+pa_status pa_decode_work(float *partial_out, float *partial_lse, const int32_t *items,
+                         int32_t num_items, int32_t max_slots, const void *q, const void *k_pool,
+                         const void *v_pool, const int32_t *block_table,
+                         int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t num_seqs,
+                         int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                         int32_t block_size, int32_t num_pages, float scale, pa_dtype dtype,
+                         int32_t *dev_err, pa_stream_t stream) {
+  pa_status st = check_read_shape(max_blocks_per_seq, num_seqs, num_q_heads, num_kv_heads,
+                                  head_dim, block_size, num_pages, scale, dtype);
+  if (st != PA_OK) return st;
+  if (!pa::mma_supports(dtype, head_dim, num_q_heads / num_kv_heads)) return PA_ERR_UNSUPPORTED;
+  if (max_slots <= 0 || max_slots > 32767 || num_items < 0) return PA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(num_items) * num_kv_heads > INT32_MAX) return PA_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return PA_OK;
+  if (num_items == 0) return PA_ERR_INVALID_ARG;  // every sequence needs an item
+  if (!partial_out || !partial_lse || !items || !q || !k_pool || !v_pool || !block_table ||
+      !seq_lens)
+    return PA_ERR_INVALID_ARG;
+  if (!aligned16(items) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) ||
+      !aligned16(partial_out))
+    return PA_ERR_INVALID_ARG;
+  pa::DecodeParams p = make_params(q, k_pool, v_pool, block_table, max_blocks_per_seq, seq_lens,
+                                   num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                   num_pages, scale, dev_err);
+  p.partial_out = partial_out;
+  p.partial_lse = partial_lse;
+  p.pages_per_split = 0;
+  p.num_splits = max_slots;
+  p.items = items;
+  p.num_items = num_items;
+  return launched(pa::launch_decode_items(p, dtype, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 pa_status pa_decode_chunk(void *out, const void *q, const void *k_pool, const void *v_pool,
                           const int32_t *block_table, int32_t max_blocks_per_seq,
                           const int32_t *seq_lens, int32_t num_seqs, int32_t chunk_len,

@@ -121,7 +121,7 @@ __device__ __forceinline__ uint32_t tile_off(int row, int chunk) {
   return row * Shape<D, NT>::kPitch + ((chunk ^ (row & 7)) << 4);
 }
 
-template <typename T, int D, int NT, bool MULTI>
+template <typename T, int D, int NT, bool MULTI, bool ITEMS>
 __global__ void __launch_bounds__(kThreads)
     decode_mma_kernel(const DecodeParams p) {
   using S = Shape<D, NT>;
@@ -137,29 +137,57 @@ __global__ void __launch_bounds__(kThreads)
 
   const int hkv = p.num_kv_heads;
   const int g = blockIdx.x % hkv;
-  const int s0 = (blockIdx.x / hkv) * p.splits_per_cta;  // first split of this CTA
-  const int nsplit = min(p.splits_per_cta, p.num_splits - s0);
-  const int b = blockIdx.y;
   const int G = p.group;
   const int bs_log2 = p.block_size_log2;
   const int bs_mask = (1 << bs_log2) - 1;
+  const long long cap = static_cast<long long>(p.max_blocks) << bs_log2;
 
   if (tid == 0) s_bad = 0u;
   pdl_wait();
+
+  // What this CTA reads: split s0 (and the next nsplit - 1) of sequence b,
+  // tokens [lo, lo + nsplit * span); in the work-list read, one item.
+  int b, s0, nsplit;
+  long long lo, span;
+  if constexpr (ITEMS) {
+    const int4 it = __ldg(reinterpret_cast<const int4 *>(p.items) + blockIdx.x / hkv);
+    const int slot = it.w & 0xffff, count = it.w >> 16;
+    if (it.x < 0 || it.x >= p.num_seqs || it.y < 0 || it.z < it.y || slot >= count ||
+        count > p.num_splits) {
+      if (tid == 0) report_error(p.dev_err, PA_DEV_BAD_ITEM);
+      return;  // the whole CTA: nothing it could write is known to be its own
+    }
+    b = it.x;
+    s0 = slot;
+    nsplit = 1;
+    lo = it.y;
+    span = static_cast<long long>(it.z) - it.y;
+    if (slot == count - 1) {
+      // the sequence's last item marks its unused slots empty
+      for (int idx = tid; idx < G * (p.num_splits - count); idx += kThreads) {
+        const int h = idx / (p.num_splits - count);
+        const int s = count + idx - h * (p.num_splits - count);
+        const size_t qh = static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(g) * G + h;
+        p.partial_lse[qh * p.num_splits + s] = -CUDART_INF_F;
+      }
+    }
+  } else {
+    b = blockIdx.y;
+    s0 = (blockIdx.x / hkv) * p.splits_per_cta;  // first split of this CTA
+    nsplit = min(p.splits_per_cta, p.num_splits - s0);
+    span = p.pages_per_split > 0 ? static_cast<long long>(p.pages_per_split) << bs_log2 : cap;
+    lo = p.pages_per_split > 0 ? static_cast<long long>(s0) * span : 0;
+  }
 
   // The prologue issues its independent loads together: the length, q, and
   // the page ids of this warp's first tiles (read speculatively from the
   // split's first position, index clamped inside the row, validated below).
   const int32_t *bt_row = p.block_table + static_cast<size_t>(b) * p.max_blocks;
-  const long long cap = static_cast<long long>(p.max_blocks) << bs_log2;
-  const long long span =
-      p.pages_per_split > 0 ? static_cast<long long>(p.pages_per_split) << bs_log2 : cap;
-  const long long lo = p.pages_per_split > 0 ? static_cast<long long>(s0) * span : 0;
   int pid_pre[S::kStages];
 #pragma unroll
   for (int s = 0; s < S::kStages; ++s) {
     const long long pos = lo + (warp + s * kWarps) * kTile + (lane & (kTile - 1));
-    pid_pre[s] = __ldg(bt_row + ((pos < cap ? pos : cap - 1) >> bs_log2));
+    pid_pre[s] = __ldg(bt_row + ((pos < cap ? (pos > 0 ? pos : 0) : cap - 1) >> bs_log2));
   }
   int len = __ldg(p.seq_lens + b);
 
@@ -481,7 +509,7 @@ __global__ void __launch_bounds__(kThreads)
     __syncthreads();
 
     const bool bad = bad_len || (s_bad != 0u);
-    const bool is_split = p.pages_per_split > 0;
+    const bool is_split = ITEMS || p.pages_per_split > 0;
     for (int idx = tid; idx < G * D; idx += kThreads) {
       const int h = idx / D;
       const int d = idx - h * D;
@@ -515,8 +543,8 @@ __global__ void __launch_bounds__(kThreads)
 template <typename T, int D, int NT>
 cudaError_t launch_shape(DecodeParams p, cudaStream_t stream) {
   using S = Shape<D, NT>;
-  auto kern = decode_mma_kernel<T, D, NT, false>;
-  auto kern_multi = decode_mma_kernel<T, D, NT, true>;
+  auto kern = decode_mma_kernel<T, D, NT, false, false>;
+  auto kern_multi = decode_mma_kernel<T, D, NT, true, false>;
   p.splits_per_cta = 1;
   p.comb_heads = S::kHeads;
   int smem = S::kSmemBytes;
@@ -556,8 +584,23 @@ cudaError_t launch_shape(DecodeParams p, cudaStream_t stream) {
   return launch_pdl(kern, grid, dim3(kThreads), smem, stream, p);
 }
 
+template <typename T, int D, int NT>
+cudaError_t launch_items_shape(const DecodeParams &p, cudaStream_t stream) {
+  using S = Shape<D, NT>;
+  auto kern = decode_mma_kernel<T, D, NT, false, true>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+  if (err != cudaSuccess) return err;
+  dim3 grid(p.num_items * p.num_kv_heads, 1);
+  return launch_pdl(kern, grid, dim3(kThreads), S::kSmemBytes, stream, p);
+}
+
 template <typename T, int D>
 cudaError_t launch_d(const DecodeParams &p, cudaStream_t stream) {
+  if (p.items != nullptr) {
+    if (p.group <= 8) return launch_items_shape<T, D, 1>(p, stream);
+    return launch_items_shape<T, D, 2>(p, stream);
+  }
   if (p.group <= 8) return launch_shape<T, D, 1>(p, stream);
   return launch_shape<T, D, 2>(p, stream);
 }
@@ -584,6 +627,10 @@ bool mma_supports(pa_dtype dtype, int head_dim, int group) {
     case 32: case 48: case 64: case 96: case 128: case 256: return true;
   }
   return false;
+}
+
+cudaError_t launch_decode_items(const DecodeParams &p, pa_dtype dtype, cudaStream_t stream) {
+  return launch_decode_mma(p, dtype, stream);  // p.items selects the work-list variant
 }
 
 cudaError_t launch_decode_mma(const DecodeParams &p, pa_dtype dtype, cudaStream_t stream) {

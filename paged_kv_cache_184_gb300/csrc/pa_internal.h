@@ -48,6 +48,8 @@ struct DecodeParams {
   int32_t num_splits;       // splits per sequence, the partials' split stride (1 if unsplit)
   int32_t splits_per_cta;   // consecutive splits one CTA reads (tensor-core read; else 1)
   int32_t comb_heads;       // head slots per warp in the combine area (tensor-core read)
+  const int32_t *items;     // work list [num_items][4] (pa_decode_work), else null
+  int32_t num_items;
   float scale_log2;         // scale * log2(e): scores kept in base-2 units
 };
 
@@ -84,6 +86,8 @@ cudaError_t launch_decode_simt(const DecodeParams &p, pa_dtype dtype, cudaStream
 // Tensor-core read: f16/bf16, head_dim in {32, 48, 64, 96, 128, 256}, groups of up to 16.
 bool mma_supports(pa_dtype dtype, int head_dim, int group);
 cudaError_t launch_decode_mma(const DecodeParams &p, pa_dtype dtype, cudaStream_t stream);
+// Tensor-core read over a planned work list (p.items), same shapes as above.
+cudaError_t launch_decode_items(const DecodeParams &p, pa_dtype dtype, cudaStream_t stream);
 // Chunked multi-query read: f16/bf16, head_dim in {32, 48, 64, 96, 128}.
 bool chunk_supports(pa_dtype dtype, int head_dim);
 int chunk_rows_per_cta();

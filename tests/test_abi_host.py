@@ -200,3 +200,22 @@ def test_chunk_validation(lib, kw, want):
                                    a["b"], a["nq"], a["hq"], a["hkv"], a["d"], a["bs"], a["np_"],
                                    a["scale"], a["dt"], None, None)
     assert st == want
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(dt=pa.PA_F32), pa.PA_ERR_UNSUPPORTED),          # tensor-core read only
+    (dict(slots=0), pa.PA_ERR_INVALID_ARG),
+    (dict(slots=40000), pa.PA_ERR_INVALID_ARG),
+    (dict(n=0), pa.PA_ERR_INVALID_ARG),                   # every sequence needs an item
+    (dict(items=MISALIGNED), pa.PA_ERR_INVALID_ARG),
+    (dict(b=0), pa.PA_OK),
+])
+def test_work_validation(lib, kw, want):
+    a = dict(po=FAKE, pl=FAKE, items=FAKE, n=10, slots=4, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, mb=4,
+             sl=FAKE, b=2, hq=8, hkv=2, d=64, bs=16, np_=32, scale=0.125, dt=pa.PA_BF16)
+    a.update(kw)
+    st = lib.raw().pa_decode_work(a["po"], a["pl"], a["items"], a["n"], a["slots"], a["q"],
+                                  a["k"], a["v"], a["bt"], a["mb"], a["sl"], a["b"], a["hq"],
+                                  a["hkv"], a["d"], a["bs"], a["np_"], a["scale"], a["dt"],
+                                  None, None)
+    assert st == want
