@@ -88,8 +88,10 @@ __device__ __forceinline__ uint32_t toff(int row, int chunk) {
   return row * ChunkShape<D>::kPitch + ((chunk ^ (row & 7)) << 4);
 }
 
+// Up to head_dim 64, 128 registers keep 4 CTAs (512 threads) per SM, which
+// measured faster than the unbounded allocation; wider heads need more.
 template <typename T, int D>
-__global__ void __launch_bounds__(kThreads) chunk_kernel(const ChunkParams p) {
+__global__ void __launch_bounds__(kThreads, D <= 64 ? 4 : 1) chunk_kernel(const ChunkParams p) {
   using S = ChunkShape<D>;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ int s_bad;
@@ -138,15 +140,20 @@ __global__ void __launch_bounds__(kThreads) chunk_kernel(const ChunkParams p) {
     const bool va = ra < rows_total, vb = rb < rows_total;
     const T *pa_ = va ? qptr(ra) : qb;
     const T *pb_ = vb ? qptr(rb) : qb;
+    // a negative scale is applied as a sign flip of q, so the scale that
+    // scores meet is never negative (the running max stays a max)
+    const uint32_t flip = p.scale_log2 < 0.f ? 0x80008000u : 0u;
 #pragma unroll
     for (int ks = 0; ks < S::kSteps; ++ks) {
       const int d0 = ks * 16 + 2 * c;
-      qa[ks][0] = va ? __ldg(reinterpret_cast<const uint32_t *>(pa_ + d0)) : 0u;
-      qa[ks][1] = vb ? __ldg(reinterpret_cast<const uint32_t *>(pb_ + d0)) : 0u;
-      qa[ks][2] = va ? __ldg(reinterpret_cast<const uint32_t *>(pa_ + d0 + 8)) : 0u;
-      qa[ks][3] = vb ? __ldg(reinterpret_cast<const uint32_t *>(pb_ + d0 + 8)) : 0u;
+      qa[ks][0] = va ? __ldg(reinterpret_cast<const uint32_t *>(pa_ + d0)) ^ flip : 0u;
+      qa[ks][1] = vb ? __ldg(reinterpret_cast<const uint32_t *>(pb_ + d0)) ^ flip : 0u;
+      qa[ks][2] = va ? __ldg(reinterpret_cast<const uint32_t *>(pa_ + d0 + 8)) ^ flip : 0u;
+      qa[ks][3] = vb ? __ldg(reinterpret_cast<const uint32_t *>(pb_ + d0 + 8)) ^ flip : 0u;
     }
   }
+  // smallest causal limit among this warp's rows: tiles ending at or below it need no mask
+  const int warp_min_pos = past + row0 / G;
 
   const int32_t *bt_row = p.block_table + static_cast<size_t>(b) * p.max_blocks;
   const T *kpool = static_cast<const T *>(p.k_pool);
@@ -197,7 +204,9 @@ __global__ void __launch_bounds__(kThreads) chunk_kernel(const ChunkParams p) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) o[n][e] = 0.f;
   float m_a = -CUDART_INF_F, m_b = -CUDART_INF_F, l_a = 0.f, l_b = 0.f;
-  const float sl2 = p.scale_log2;
+  // |scale| * log2(e), kept at least 1e-30 so that a masked score (-inf) times it
+  // stays -inf when scale is 0; raw scores times 1e-30 are 0 to fp32 precision
+  const float sl2 = fmaxf(fabsf(p.scale_log2), 1e-30f);
 
   for (int j = 0; j < ntiles; ++j) {
     cp_async_wait<kStages - 2>();
@@ -233,15 +242,21 @@ __global__ void __launch_bounds__(kThreads) chunk_kernel(const ChunkParams p) {
       }
     }
 
-    // causal mask, scale to base 2, row max over the tile
+    // causal mask (only on tiles that cross a row's limit) and the row max,
+    // in raw score units; the scale is applied inside the exponent below
+    if (tok0 + kKeyTile - 1 > warp_min_pos) {
+#pragma unroll
+      for (int n = 0; n < 8; ++n) {
+        const int t = tok0 + n * 8 + 2 * c;
+        if (t > pos_a) sc[n][0] = -CUDART_INF_F;
+        if (t + 1 > pos_a) sc[n][1] = -CUDART_INF_F;
+        if (t > pos_b) sc[n][2] = -CUDART_INF_F;
+        if (t + 1 > pos_b) sc[n][3] = -CUDART_INF_F;
+      }
+    }
     float mx_a = -CUDART_INF_F, mx_b = -CUDART_INF_F;
 #pragma unroll
     for (int n = 0; n < 8; ++n) {
-      const int t = tok0 + n * 8 + 2 * c;
-      sc[n][0] = (t <= pos_a) ? sc[n][0] * sl2 : -CUDART_INF_F;
-      sc[n][1] = (t + 1 <= pos_a) ? sc[n][1] * sl2 : -CUDART_INF_F;
-      sc[n][2] = (t <= pos_b) ? sc[n][2] * sl2 : -CUDART_INF_F;
-      sc[n][3] = (t + 1 <= pos_b) ? sc[n][3] * sl2 : -CUDART_INF_F;
       mx_a = fmaxf(mx_a, fmaxf(sc[n][0], sc[n][1]));
       mx_b = fmaxf(mx_b, fmaxf(sc[n][2], sc[n][3]));
     }
@@ -251,18 +266,19 @@ __global__ void __launch_bounds__(kThreads) chunk_kernel(const ChunkParams p) {
       mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, off));
     }
     const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
-    const float mu_a = mn_a == -CUDART_INF_F ? 0.f : mn_a;
-    const float mu_b = mn_b == -CUDART_INF_F ? 0.f : mn_b;
-    const float al_a = exp2f(m_a - mu_a), al_b = exp2f(m_b - mu_b);
+    const float mu_a = mn_a == -CUDART_INF_F ? 0.f : mn_a * sl2;  // scaled max
+    const float mu_b = mn_b == -CUDART_INF_F ? 0.f : mn_b * sl2;
+    const float al_a = m_a == -CUDART_INF_F ? 0.f : ex2_approx(fmaf(m_a, sl2, -mu_a));
+    const float al_b = m_b == -CUDART_INF_F ? 0.f : ex2_approx(fmaf(m_b, sl2, -mu_b));
     m_a = mn_a;
     m_b = mn_b;
     float sum_a = 0.f, sum_b = 0.f;
 #pragma unroll
     for (int n = 0; n < 8; ++n) {
-      sc[n][0] = exp2f(sc[n][0] - mu_a);
-      sc[n][1] = exp2f(sc[n][1] - mu_a);
-      sc[n][2] = exp2f(sc[n][2] - mu_b);
-      sc[n][3] = exp2f(sc[n][3] - mu_b);
+      sc[n][0] = ex2_approx(fmaf(sc[n][0], sl2, -mu_a));  // exp2(-inf) = 0 for masked keys
+      sc[n][1] = ex2_approx(fmaf(sc[n][1], sl2, -mu_a));
+      sc[n][2] = ex2_approx(fmaf(sc[n][2], sl2, -mu_b));
+      sc[n][3] = ex2_approx(fmaf(sc[n][3], sl2, -mu_b));
       sum_a += sc[n][0] + sc[n][1];
       sum_b += sc[n][2] + sc[n][3];
     }

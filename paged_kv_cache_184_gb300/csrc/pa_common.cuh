@@ -23,6 +23,14 @@ __device__ __forceinline__ void report_error(int32_t *dev_err, int32_t code) {
   if (dev_err != nullptr) atomicCAS(dev_err, 0, code);
 }
 
+// 2^x by the SFU's approximate base-2 exponential (relative error about
+// 2^-22; 2^-inf = +0, subnormal results flush to zero).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ---- 16-byte chunk -> fp32 ------------------------------------------------
 
 template <typename T> struct Elem;

@@ -101,3 +101,13 @@ def test_bad_page_is_reported_and_zeroed(lib):
     assert int(err.item()) == 1
     assert torch.all(out[3] == 0)
     assert_attn_close(out[:3], _ref(base, q, [0, 1, 2]), base.dtype)
+
+
+@pytest.mark.parametrize("scale", [-0.125, 0.0, 0.7])
+def test_any_finite_scale(lib, scale):
+    # a negative scale runs as a sign flip of q; scale 0 gives the mean of the visible V rows
+    base = workloads.awkward()
+    base.scale = scale
+    q = _chunk_batch(base, 5)
+    out = _run(lib, base, q)
+    assert_attn_close(out, _ref(base, q), base.dtype, f"scale {scale}")
