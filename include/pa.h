@@ -71,7 +71,8 @@ enum {
   PA_DEV_BAD_POSITION = 2, /* append position outside [0, max_blocks_per_seq * block_size) */
   PA_DEV_BAD_SEQ_LEN = 3,  /* seq_len outside [0, max_blocks_per_seq * block_size] */
   PA_DEV_BAD_SEQ_ID = 4,   /* append seq id outside [0, num_seqs) */
-  PA_DEV_BAD_ITEM = 5      /* work item with a bad sequence, range or slot */
+  PA_DEV_BAD_ITEM = 5,     /* work item with a bad sequence, range or slot */
+  PA_DEV_TIMEOUT = 6       /* a bounded wait for the tensor cores ran out (output zeroed) */
 };
 
 /* Human-readable name of a status code (static string). */
@@ -232,9 +233,12 @@ pa_status pa_decode_work(float *partial_out, float *partial_lse, const int32_t *
  *   out[b][i][h] = softmax_{t <= past+i}(scale * q[b][i][h] . K_b[t][g]) @ V_b[t][g].
  * A query at a negative position (chunk_len > seq_lens[b]) sees nothing and
  * its output is 0.  q and out are [num_seqs][chunk_len][num_q_heads][head_dim].
- * chunk_len == 1 is a single-query read.  f16/bf16 only, head_dim 32, 48,
- * 64, 96 or 128 (otherwise PA_ERR_UNSUPPORTED); fp32 accumulation and
- * softmax, the probabilities rounded to the cache dtype for the P.V product.
+ * chunk_len == 1 is a single-query read; a prompt's prefill is the chunk
+ * with chunk_len == seq_lens[b].  f16/bf16 only, head_dim 32, 48, 64, 96 or
+ * 128 (otherwise PA_ERR_UNSUPPORTED); fp32 accumulation and softmax, the
+ * probabilities rounded to the cache dtype for the P.V product.  Chunks of
+ * at least 128 (query, head) rows per kv head at head_dim 64 or 128 run on
+ * the tcgen05 tensor cores, smaller ones on mma.sync.
  */
 pa_status pa_decode_chunk(void *out, const void *q, const void *k_pool,
                           const void *v_pool, const int32_t *block_table,

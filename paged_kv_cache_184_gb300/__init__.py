@@ -24,7 +24,7 @@ LIB_PATH = _build.LIB_PATH
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA = 0, 1, 2, 3
 PA_F32, PA_F16, PA_BF16 = 0, 1, 2
 PA_DEV_OK, PA_DEV_BAD_PAGE, PA_DEV_BAD_POSITION, PA_DEV_BAD_SEQ_LEN, PA_DEV_BAD_SEQ_ID = 0, 1, 2, 3, 4
-PA_DEV_BAD_ITEM = 5
+PA_DEV_BAD_ITEM, PA_DEV_TIMEOUT = 5, 6
 
 EXPORTED = ("pa_status_string", "pa_version", "pa_num_splits", "pa_cache_append",
             "pa_decode", "pa_decode_splitkv", "pa_merge", "pa_decode_splitkv_noalloc",

@@ -272,7 +272,10 @@ pa_status pa_decode_chunk(void *out, const void *q, const void *k_pool, const vo
   p.block_size_log2 = log2_exact(block_size);
   p.num_pages = num_pages;
   p.scale_log2 = scale * 1.4426950408889634f;
-  return launched(pa::launch_chunk(p, dtype, reinterpret_cast<cudaStream_t>(stream)));
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (pa::chunk_tc_supports(dtype, head_dim, static_cast<int>(rows)))
+    return launched(pa::launch_chunk_tc(p, dtype, s));
+  return launched(pa::launch_chunk(p, dtype, s));
 }
 
 pa_status pa_merge(void *out, const float *partial_out, const float *partial_lse,

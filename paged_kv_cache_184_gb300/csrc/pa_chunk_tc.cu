@@ -1,0 +1,434 @@
+// Chunked multi-query / prefill read on the 5th-generation tensor cores
+// (tcgen05.mma, accumulators in tensor memory).
+//
+// Same contract as the mma.sync chunk read (nanoserve "Day 23: the real
+// triton.jit paged-attention kernel": query i of a chunk sits at position
+// past + i and sees tokens 0 .. past + i), for chunks long enough to fill
+// 128-row tiles: a prompt's prefill is the chunk that starts at past = 0.
+// One CTA owns 128 (query, head) rows of one (sequence, kv head), one row
+// per thread, and walks the causal key range in 64-token tiles:
+//
+//   S [128 x 64] = Q [128 x D] . K_tile^T      tcgen05.mma -> tensor memory
+//   softmax      : thread r loads row r of S (tcgen05.ld), masks, takes the
+//                  running max and sum in fp32, and writes P (bf16/f16) in
+//                  the 128-byte-swizzled K-major layout over the K tile it
+//                  no longer needs
+//   O [128 x D] += P . V_tile                 tcgen05.mma, O stays in tensor memory
+//
+// The running max used for the exponent is only moved when a row's max
+// grows by more than 2^8 (then O and l are rescaled, warp by warp, through
+// tcgen05.ld/st); otherwise P values up to 2^8 are used as they are.  O and
+// l always share the same reference max, so the result is the same softmax.
+//
+// K/V tiles come through the block table ("Three Attention Kernels",
+// section "3. Paged KV-cache attention") with 16-byte cp.async copies into
+// the swizzled layouts the tensor core reads (K: K-major, V: MN-major), two
+// tiles in flight.  Thread 0 issues the MMAs; completion is signalled on an
+// mbarrier by tcgen05.commit, and every wait on it is bounded: on time-out
+// the kernel records PA_DEV_TIMEOUT, waits (bounded) no further, frees its
+// tensor memory and leaves.
+#include <math_constants.h>
+
+#include <type_traits>
+
+#include "pa_common.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+constexpr int kRows = 128;      // rows per CTA (the MMA M), one per thread
+constexpr int kThreads = 128;
+constexpr int kKeyTile = 64;    // tokens per tile (the QK MMA N, the PV MMA K)
+constexpr uint32_t kSpinLimit = 1u << 26;
+constexpr float kRescaleLog2 = 8.f;  // move the reference max when it grows by more than 2^8
+
+template <int D>
+struct TcShape {
+  static constexpr int kKB = D / 64;                    // 64-element swizzle atoms along D
+  static constexpr int kQBytes = kRows * D * 2;         // Q: [kb][128 rows][128 B]
+  static constexpr int kKVBytes = kKeyTile * D * 2;     // one K or V tile: [kb][64 rows][128 B]
+  static constexpr int kPBytes = kRows * kKeyTile * 2;  // P: [128 rows][128 B]
+  // P reuses the K buffer of its tile when that is large enough (D >= 128)
+  static constexpr bool kPInK = kKVBytes >= kPBytes;
+  static constexpr int kSmem = kQBytes + 4 * kKVBytes + (kPInK ? 0 : kPBytes) + 1024;
+  static constexpr int kTmemCols = (kKeyTile + D) <= 128 ? 128 : 256;  // S then O
+};
+
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = static_cast<uint64_t>((saddr >> 4) & 0x3FFF);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFF) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFF) << 32;
+  d |= static_cast<uint64_t>(1) << 46;  // descriptor version of this architecture
+  d |= static_cast<uint64_t>(2) << 61;  // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulate, A/B element type,
+// A K-major, B K-major or MN-major, N and M.
+template <typename T>
+__host__ __device__ constexpr uint32_t idesc(int m, int n, bool b_mn_major) {
+  const uint32_t ab = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
+  return (1u << 4) | (ab << 7) | (ab << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t id,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(tmem_d),
+      "l"(da), "l"(db), "r"(id), "r"(accumulate));
+}
+
+__device__ __forceinline__ void commit(uint32_t mbar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   mbar)
+               : "memory");
+}
+
+// Wait for the given phase of an mbarrier; false after kSpinLimit polls.
+__device__ __forceinline__ bool wait_phase(uint32_t mbar, uint32_t phase) {
+  for (uint32_t it = 0; it < kSpinLimit; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(done)
+        : "r"(mbar), "r"(phase)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float *v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]),
+      "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]),
+      "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]),
+      "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]),
+      "f"(v[29]), "f"(v[30]), "f"(v[31]));
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+template <typename T> struct Pack2;
+template <> struct Pack2<__nv_bfloat16> {
+  __device__ __forceinline__ static uint32_t run(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+  }
+};
+template <> struct Pack2<__half> {
+  __device__ __forceinline__ static uint32_t run(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+  }
+};
+
+// byte offset of 16-byte chunk `chunk` of row `row` in a [kb][rows][128 B] swizzled tile
+__device__ __forceinline__ uint32_t sw_off(int row, int chunk, int rows) {
+  return (chunk >> 3) * rows * 128 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads) chunk_tc_kernel(const ChunkParams p) {
+  using S = TcShape<D>;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ uint64_t mbar_s, mbar_o;
+  __shared__ uint32_t tmem_base;
+  __shared__ int s_bad, s_fail;
+
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int hkv = p.num_kv_heads, G = p.group, nq = p.chunk_len;
+  const int g = blockIdx.x % hkv;
+  const int rows_total = nq * G;
+  const int nblk = (rows_total + kRows - 1) / kRows;
+  const int rblk = nblk - 1 - blockIdx.x / hkv;  // the longest causal ranges start first
+  const int b = blockIdx.y;
+  const int bs_log2 = p.block_size_log2, bs_mask = (1 << bs_log2) - 1;
+
+  unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  unsigned char *sq = smem;                     // Q
+  unsigned char *skv = smem + S::kQBytes;       // K0, V0, K1, V1
+  unsigned char *sp_own = skv + 4 * S::kKVBytes;  // P when it cannot live in K
+
+  if (tid == 0) {
+    s_bad = 0;
+    s_fail = 0;
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&mbar_s)));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&mbar_o)));
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&tmem_base)),
+                 "n"(S::kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  pdl_wait();
+
+  int len = __ldg(p.seq_lens + b);
+  const long long cap = static_cast<long long>(p.max_blocks) << bs_log2;
+  const bool bad_len = (len < 0) || (static_cast<long long>(len) > cap);
+  if (bad_len) len = 0;
+  const int past = len - nq;
+  const int row = rblk * kRows + tid;  // this thread's row
+  const bool row_ok = row < rows_total;
+  const int pos = past + row / G;      // its causal limit (inclusive)
+  const int last_row = min(rows_total - 1, rblk * kRows + kRows - 1);
+  const int kv_end = max(0, min(len, past + last_row / G + 1));
+  const int ntiles = (kv_end + kKeyTile - 1) / kKeyTile;
+
+  // ---- Q rows into the swizzled K-major layout ----------------------------
+  const T *qbase = static_cast<const T *>(p.q);
+  for (int idx = tid; idx < kRows * (D / 8); idx += kThreads) {
+    const int r = idx / (D / 8), c = idx - r * (D / 8);
+    const int qr = rblk * kRows + r;
+    const bool ok = qr < rows_total;
+    const T *src = qbase;
+    if (ok) {
+      const int i = qr / G, h = qr - (qr / G) * G;
+      src = qbase + ((static_cast<size_t>(b) * nq + i) * p.num_q_heads +
+                     static_cast<size_t>(g) * G + h) * D + c * 8;
+    }
+    cp_async16(sq + sw_off(r, c, kRows), src, ok);
+  }
+  cp_async_commit();
+
+  const int32_t *bt_row = p.block_table + static_cast<size_t>(b) * p.max_blocks;
+  const T *kpool = static_cast<const T *>(p.k_pool);
+  const T *vpool = static_cast<const T *>(p.v_pool);
+  auto load_tile = [&](int j, int stage) {
+    unsigned char *ks = skv + (2 * stage) * S::kKVBytes;
+    unsigned char *vs = ks + S::kKVBytes;
+    for (int idx = tid; idx < kKeyTile * (D / 8); idx += kThreads) {
+      const int tr = idx / (D / 8), c = idx - tr * (D / 8);
+      const int t = j * kKeyTile + tr;
+      bool valid = t < kv_end;
+      const T *ksrc = kpool, *vsrc = vpool;
+      if (valid) {
+        const int page = __ldg(bt_row + (t >> bs_log2));
+        if (page < 0 || page >= p.num_pages) {
+          report_error(p.dev_err, PA_DEV_BAD_PAGE);
+          s_bad = 1;
+          valid = false;
+        } else {
+          const size_t off =
+              (((static_cast<size_t>(page) << bs_log2) + (t & bs_mask)) * hkv + g) * D + c * 8;
+          ksrc += off;
+          vsrc += off;
+        }
+      }
+      const uint32_t o = sw_off(tr, c, kKeyTile);
+      cp_async16(ks + o, ksrc, valid);
+      cp_async16(vs + o, vsrc, valid);
+    }
+  };
+  if (ntiles > 0) load_tile(0, 0);
+  cp_async_commit();
+
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();  // barrier init, tensor-memory address, s_bad
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = tmem_base;
+  const uint32_t t_lane = static_cast<uint32_t>(warp * 32) << 16;  // this warp's 32 lanes
+  const uint32_t t_s = tmem, t_o = tmem + kKeyTile;
+  const uint32_t id_qk = idesc<T>(kRows, kKeyTile, false);
+  const uint32_t id_pv = idesc<T>(kRows, D, true);
+
+  const float sl2 = fmaxf(fabsf(p.scale_log2), 1e-30f);
+  const bool neg = p.scale_log2 < 0.f;  // a negative scale flips every score's sign
+  float m_ref = -CUDART_INF_F;          // reference max (raw units) of the exponent
+  float l = 0.f;
+  bool fail = false;
+
+  for (int j = 0; j < ntiles; ++j) {
+    const int stage = j & 1;
+    if (j + 1 < ntiles) load_tile(j + 1, stage ^ 1);
+    cp_async_commit();
+    cp_async_wait<1>();  // Q and tile j are in shared memory
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor core
+    __syncthreads();
+    const uint32_t ks_u = smem_u32(skv + (2 * stage) * S::kKVBytes);
+    const uint32_t vs_u = ks_u + S::kKVBytes;
+    const uint32_t ps_u = S::kPInK ? ks_u : smem_u32(sp_own);
+
+    // S = Q . K^T
+    if (tid == 0) {
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const uint32_t kb = ks >> 2, kin = (ks & 3) * 32;
+        mma_f16(t_s, sw128_desc(smem_u32(sq) + kb * (kRows * 128) + kin, 16, 1024),
+                sw128_desc(ks_u + kb * (kKeyTile * 128) + kin, 16, 1024), id_qk, ks > 0);
+      }
+      commit(smem_u32(&mbar_s));
+    }
+    if (!wait_phase(smem_u32(&mbar_s), j & 1)) fail = true;
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+
+    // row `row` of S: mask, running max, probabilities
+    float s[kKeyTile];
+    tmem_ld32(t_s + t_lane, s);
+    tmem_ld32(t_s + t_lane + 32, s + 32);
+    const int tok0 = j * kKeyTile;
+    float mx = -CUDART_INF_F;
+#pragma unroll
+    for (int c = 0; c < kKeyTile; ++c) {
+      const float v = neg ? -s[c] : s[c];
+      s[c] = (tok0 + c <= pos) ? v : -CUDART_INF_F;
+      mx = fmaxf(mx, s[c]);
+    }
+    float alpha = 1.f;
+    if (mx != -CUDART_INF_F &&
+        (m_ref == -CUDART_INF_F || (mx - m_ref) * sl2 > kRescaleLog2)) {
+      alpha = m_ref == -CUDART_INF_F ? 0.f : ex2_approx((m_ref - mx) * sl2);
+      m_ref = mx;
+    }
+    const float mu = m_ref == -CUDART_INF_F ? 0.f : m_ref * sl2;
+    float sum = 0.f;
+#pragma unroll
+    for (int c = 0; c < kKeyTile; ++c) {
+      s[c] = ex2_approx(fmaf(s[c], sl2, -mu));  // masked: 2^-inf = 0
+      sum += s[c];
+    }
+    l = fmaf(l, alpha, sum);
+    // P row into the K-major swizzled tile, over the K tile when it fits: every
+    // thread has seen the QK product complete (mbarrier above) before writing
+#pragma unroll
+    for (int c = 0; c < kKeyTile / 8; ++c) {
+      uint4 w;
+      w.x = Pack2<T>::run(s[8 * c + 0], s[8 * c + 1]);
+      w.y = Pack2<T>::run(s[8 * c + 2], s[8 * c + 3]);
+      w.z = Pack2<T>::run(s[8 * c + 4], s[8 * c + 5]);
+      w.w = Pack2<T>::run(s[8 * c + 6], s[8 * c + 7]);
+      *reinterpret_cast<uint4 *>((S::kPInK ? skv + (2 * stage) * S::kKVBytes : sp_own) +
+                                 tid * 128 + ((c ^ (tid & 7)) << 4)) = w;
+    }
+    // rescale this warp's O rows when any of them moved its reference max
+    if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+      for (int cb = 0; cb < D; cb += 32) {
+        float o[32];
+        tmem_ld32(t_o + t_lane + cb, o);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] *= alpha;
+        tmem_st32(t_o + t_lane + cb, o);
+      }
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+
+    // O += P . V
+    if (tid == 0) {
+#pragma unroll
+      for (int kk = 0; kk < kKeyTile / 16; ++kk) {
+        mma_f16(t_o, sw128_desc(ps_u + kk * 32, 16, 1024),
+                sw128_desc(vs_u + kk * 2048, kKeyTile * 128, 1024), id_pv, (j > 0 || kk > 0));
+      }
+      commit(smem_u32(&mbar_o));
+    }
+    if (!wait_phase(smem_u32(&mbar_o), j & 1)) fail = true;
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (__syncthreads_or(fail)) {
+      fail = true;
+      break;
+    }
+  }
+  cp_async_wait_all();
+  pdl_trigger();
+
+  // ---- epilogue: O / l to the output --------------------------------------
+  if (fail && tid == 0) report_error(p.dev_err, PA_DEV_TIMEOUT);
+  __syncthreads();
+  const bool bad = bad_len || s_bad != 0 || fail;
+  const bool have_o = ntiles > 0 && !fail;  // uniform over the CTA
+  T *dst = static_cast<T *>(p.out);
+  if (row_ok) {
+    const int i = row / G, h = row - (row / G) * G;
+    dst += ((static_cast<size_t>(b) * nq + i) * p.num_q_heads + static_cast<size_t>(g) * G + h) * D;
+  }
+  const float inv = (bad || l == 0.f || !have_o) ? 0.f : 1.f / l;
+#pragma unroll
+  for (int cb = 0; cb < D; cb += 32) {
+    float o[32];
+    if (have_o) {
+      tmem_ld32(t_o + t_lane + cb, o);  // all lanes: the load is warp-collective
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) o[e] = 0.f;
+    }
+    if (row_ok) {
+#pragma unroll
+      for (int e = 0; e < 32; e += 8) {
+        uint4 w;
+        w.x = Pack2<T>::run(o[e] * inv, o[e + 1] * inv);
+        w.y = Pack2<T>::run(o[e + 2] * inv, o[e + 3] * inv);
+        w.z = Pack2<T>::run(o[e + 4] * inv, o[e + 5] * inv);
+        w.w = Pack2<T>::run(o[e + 6] * inv, o[e + 7] * inv);
+        *reinterpret_cast<uint4 *>(dst + cb + e) = w;
+      }
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 0) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "n"(S::kTmemCols));
+  }
+}
+
+template <typename T, int D>
+cudaError_t launch_d(const ChunkParams &p, cudaStream_t stream) {
+  auto kern = chunk_tc_kernel<T, D>;
+  const int smem = TcShape<D>::kSmem;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  const int nblk = (p.chunk_len * p.group + kRows - 1) / kRows;
+  dim3 grid(nblk * p.num_kv_heads, p.num_seqs);
+  return launch_pdl(kern, grid, dim3(kThreads), smem, stream, p);
+}
+
+template <typename T>
+cudaError_t launch_t(const ChunkParams &p, cudaStream_t stream) {
+  switch (p.head_dim) {
+    case 64: return launch_d<T, 64>(p, stream);
+    case 128: return launch_d<T, 128>(p, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+bool chunk_tc_supports(pa_dtype dtype, int head_dim, int rows) {
+  if (dtype != PA_F16 && dtype != PA_BF16) return false;
+  if (head_dim != 64 && head_dim != 128) return false;
+  return rows >= kRows;  // at least one full 128-row tile per (sequence, kv head)
+}
+
+cudaError_t launch_chunk_tc(const ChunkParams &p, pa_dtype dtype, cudaStream_t stream) {
+  if (dtype == PA_BF16) return launch_t<__nv_bfloat16>(p, stream);
+  if (dtype == PA_F16) return launch_t<__half>(p, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pa

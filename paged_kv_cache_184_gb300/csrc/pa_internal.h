@@ -92,6 +92,10 @@ cudaError_t launch_decode_items(const DecodeParams &p, pa_dtype dtype, cudaStrea
 bool chunk_supports(pa_dtype dtype, int head_dim);
 int chunk_rows_per_cta();
 cudaError_t launch_chunk(const ChunkParams &p, pa_dtype dtype, cudaStream_t stream);
+// Its tcgen05 variant, for at least one full 128-row tile per (sequence, kv head):
+// f16/bf16, head_dim 64 or 128.
+bool chunk_tc_supports(pa_dtype dtype, int head_dim, int rows);
+cudaError_t launch_chunk_tc(const ChunkParams &p, pa_dtype dtype, cudaStream_t stream);
 cudaError_t launch_append(const AppendParams &p, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams &p, pa_dtype dtype, cudaStream_t stream);
 

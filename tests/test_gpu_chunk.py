@@ -111,3 +111,56 @@ def test_any_finite_scale(lib, scale):
     q = _chunk_batch(base, 5)
     out = _run(lib, base, q)
     assert_attn_close(out, _ref(base, q), base.dtype, f"scale {scale}")
+
+
+# ---------------------------------------------------------------- tcgen05 path (>= 128 rows)
+
+
+@pytest.mark.parametrize("dtype,hq,hkv,d,bs,n_q,lens", [
+    ("bf16", 32, 8, 64, 16, 32, [32, 100, 700, 4096]),       # 128 rows: one tile
+    ("bf16", 32, 8, 64, 16, 50, [60, 50, 333, 1000]),        # 200 rows: a partial second tile
+    ("bf16", 32, 8, 128, 16, 40, [40, 41, 500, 2049]),       # head_dim 128, P over the K tile
+    ("f16", 32, 8, 128, 8, 64, [64, 65, 129, 900]),          # fp16, pages of 8
+    ("bf16", 32, 4, 64, 32, 16, [16, 300, 777, 1500]),       # group 8
+    ("bf16", 32, 2, 128, 16, 8, [8, 9, 250, 3000]),          # group 16
+    ("f16", 16, 4, 64, 16, 48, [20, 48, 130, 640]),          # queries at negative positions
+])
+def test_tensor_core_chunks(lib, dtype, hq, hkv, d, bs, n_q, lens):
+    pages = sum(-(-n // bs) for n in lens) + 5
+    base = workloads.make_batch("tc", 41, dtype, lens, hq, hkv, d, bs, pages)
+    assert n_q * (hq // hkv) >= 128
+    q = _chunk_batch(base, n_q)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = _run(lib, base, q, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_attn_close(out, _ref(base, q), base.dtype)
+
+
+def test_tensor_core_prefill(lib):
+    # whole prompts: chunk_len == seq_len, so past == 0 and the read is causal prefill
+    base = workloads.make_batch("prefill", 43, "bf16", [200, 200, 200], 32, 8, 128, 16, 40)
+    q = _chunk_batch(base, 200)
+    out = _run(lib, base, q)
+    assert_attn_close(out, _ref(base, q), base.dtype, "prefill")
+
+
+@pytest.mark.parametrize("scale", [-0.09, 0.0, 0.6])
+def test_tensor_core_any_finite_scale(lib, scale):
+    base = workloads.make_batch("tcs", 44, "bf16", [64, 300, 90], 32, 8, 64, 16, 40)
+    base.scale = scale
+    q = _chunk_batch(base, 32)
+    out = _run(lib, base, q)
+    assert_attn_close(out, _ref(base, q), base.dtype, f"scale {scale}")
+
+
+def test_tensor_core_bad_page_is_reported_and_zeroed(lib):
+    base = workloads.make_batch("tcbad", 45, "bf16", [64, 300, 500], 32, 8, 64, 16, 60)
+    base.block_table[2, 3] = base.num_pages + 9
+    q = _chunk_batch(base, 32)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = _run(lib, base, q, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 1
+    assert torch.all(out[2] == 0)
+    assert_attn_close(out[:2], _ref(base, q, [0, 1]), base.dtype)
