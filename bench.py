@@ -56,7 +56,8 @@ def parse_args():
     ap.add_argument("--history", type=int, default=4096)
     ap.add_argument("--no-extras", action="store_true",
                     help="headline step only (no sweep, long-context, ragged, CPU baseline)")
-    ap.add_argument("--only", choices=["sweep", "longctx", "ragged8b", "dense_vs_sdpa", "chunk"],
+    ap.add_argument("--only", choices=["sweep", "longctx", "ragged8b", "dense_vs_sdpa", "chunk",
+                                       "prefill"],
                     help="run one extra section alone and print its JSON (for profiling)")
     return ap.parse_args()
 
@@ -298,7 +299,8 @@ def main():
                "longctx": lambda: longctx(pa, workloads, torch, dev, peak),
                "ragged8b": lambda: ragged(pa, workloads, torch, dev, peak),
                "dense_vs_sdpa": lambda: dense_vs_sdpa(pa, workloads, torch, dev, peak),
-               "chunk": lambda: chunk(pa, workloads, torch, dev, peak)}
+               "chunk": lambda: chunk(pa, workloads, torch, dev, peak),
+               "prefill": lambda: prefill(pa, workloads, torch, dev)}
         print(json.dumps({args.only: fns[args.only]()}), flush=True)
         return
     dist = None
@@ -447,6 +449,7 @@ def main():
         line["ragged8b"] = ragged(pa, workloads, torch, dev, peak)
         line["dense_vs_sdpa"] = dense_vs_sdpa(pa, workloads, torch, dev, peak)
         line["chunk"] = chunk(pa, workloads, torch, dev, peak)
+        line["prefill"] = prefill(pa, workloads, torch, dev)
         if world == 1:
             t, nb, n = OracleSample(cpu).run(12.0, 64)
             line["cpu_baseline"] = {
@@ -606,6 +609,45 @@ def chunk(pa, workloads, torch, dev, peak):
                      "tflops": flops / (med * 1e-3) / 1e12})
         del q, out
     del g
+    torch.cuda.empty_cache()
+    return rows
+
+
+def measured_bf16_tflops():
+    """Dense bf16 tensor peak (TFLOP/s) measured on this machine, else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            j = json.load(f)
+        for key in ("bf16_tflops", "bf16_tflops_burst"):
+            if isinstance(j.get(key), (int, float)):
+                return float(j[key]), "measured"
+    except (OSError, ValueError):
+        pass
+    return 1900.0, "fallback"
+
+
+def prefill(pa, workloads, torch, dev):
+    """Causal prefill of 8 prompts x 4096 tokens through pa_decode_chunk (chunk = the whole
+    prompt, tcgen05 path), head_dim 64 (Llama-3.2-1B heads) and 128 (Llama-3-8B heads)."""
+    flush = L2Flush(torch, dev)
+    peak_tf, kind = measured_bf16_tflops()
+    rows = []
+    for d in (64, 128):
+        g = workloads.make_batch(f"prefill_d{d}", 6, "bf16", [4096] * 8, 32, 8, d, 16, 8 * 256,
+                                 device=str(dev))
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(8)
+        q = torch.randn((8, 4096, 32, d), generator=gen, device=dev).to(torch.bfloat16)
+        out = torch.empty_like(q)
+        fn = lambda: pa.pa_decode_chunk(out, q, g.k_pool, g.v_pool, g.block_table, g.seq_lens,
+                                        g.scale)
+        med, mn = _time_launches(fn, torch, flush, iters=10)
+        flops = 8 * 4 * 32 * d * (4096 * 4097 // 2)
+        tf = flops / (med * 1e-3) / 1e12
+        rows.append({"head_dim": d, "batch": 8, "prompt": 4096, "us": 1e3 * med,
+                     "tflops": tf, "peak_tflops": peak_tf, "peak_source": kind,
+                     "frac_tensor": tf / peak_tf})
+        del g, q, out
     torch.cuda.empty_cache()
     return rows
 

@@ -164,3 +164,26 @@ def test_tensor_core_bad_page_is_reported_and_zeroed(lib):
     assert int(err.item()) == 1
     assert torch.all(out[2] == 0)
     assert_attn_close(out[:2], _ref(base, q, [0, 1]), base.dtype)
+
+
+def test_prefill_4096_sampled_rows(lib):
+    # the measured prefill launch (8 prompts x 4096 tokens, head_dim 128), checked on
+    # sampled queries of two prompts against attention over their causal prefixes
+    base = workloads.make_batch("prefill_d128", 6, "bf16", [4096] * 8, 32, 8, 128, 16, 8 * 256,
+                                device=DEV)
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(8)
+    q = torch.randn((8, 4096, 32, 128), generator=gen, device=DEV).to(torch.bfloat16)
+    out = torch.empty_like(q)
+    lib.pa_decode_chunk(out, q, base.k_pool, base.v_pool, base.block_table, base.seq_lens,
+                        base.scale)
+    torch.cuda.synchronize()
+    for b in (0, 7):
+        pages = base.block_table[b].long()
+        k = host_f32(base.k_pool.index_select(0, pages)).reshape(4096, 8, 128)
+        v = host_f32(base.v_pool.index_select(0, pages)).reshape(4096, 8, 128)
+        for i in (0, 1, 127, 128, 2000, 4095):
+            for h in (0, 5, 31):
+                ref, _ = oracle.attend(host_f32(q[b, i, h]), k[:i + 1, h // 4], v[:i + 1, h // 4],
+                                       base.scale)
+                assert_attn_close(out[b, i, h], ref, base.dtype, f"b{b} i{i} h{h}")
