@@ -45,7 +45,6 @@ constexpr float kRescaleLog2 = 8.f;  // move the reference max when it grows by 
 
 template <int D>
 struct TcShape {
-  static constexpr int kKB = D / 64;                    // 64-element swizzle atoms along D
   static constexpr int kQBytes = kRows * D * 2;         // Q: [kb][128 rows][128 B]
   static constexpr int kKVBytes = kKeyTile * D * 2;     // one K or V tile: [kb][64 rows][128 B]
   static constexpr int kPBytes = kRows * kKeyTile * 2;  // P: [128 rows][128 B]
@@ -67,10 +66,11 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
 // Instruction descriptor of kind::f16: fp32 accumulate, A/B element type,
 // A K-major, B K-major or MN-major, N and M.
 template <typename T>
-__host__ __device__ constexpr uint32_t idesc(int m, int n, bool b_mn_major) {
+__host__ __device__ constexpr uint32_t idesc(int m, int n, bool b_mn_major, bool negate_a) {
   const uint32_t ab = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
-  return (1u << 4) | (ab << 7) | (ab << 10) | ((b_mn_major ? 1u : 0u) << 16) |
-         (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+  return (1u << 4) | (ab << 7) | (ab << 10) | ((negate_a ? 1u : 0u) << 13) |
+         ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(m >> 4) << 24);
 }
 
 __device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t id,
@@ -251,11 +251,10 @@ __global__ void __launch_bounds__(kThreads) chunk_tc_kernel(const ChunkParams p)
   const uint32_t tmem = tmem_base;
   const uint32_t t_lane = static_cast<uint32_t>(warp * 32) << 16;  // this warp's 32 lanes
   const uint32_t t_s = tmem, t_o = tmem + kKeyTile;
-  const uint32_t id_qk = idesc<T>(kRows, kKeyTile, false);
-  const uint32_t id_pv = idesc<T>(kRows, D, true);
-
   const float sl2 = fmaxf(fabsf(p.scale_log2), 1e-30f);
-  const bool neg = p.scale_log2 < 0.f;  // a negative scale flips every score's sign
+  const bool neg = p.scale_log2 < 0.f;  // a negative scale negates Q . K^T in the MMA
+  const uint32_t id_qk = idesc<T>(kRows, kKeyTile, false, neg);
+  const uint32_t id_pv = idesc<T>(kRows, D, true, false);
   float m_ref = -CUDART_INF_F;          // reference max (raw units) of the exponent
   float l = 0.f;
   bool fail = false;
@@ -289,13 +288,19 @@ __global__ void __launch_bounds__(kThreads) chunk_tc_kernel(const ChunkParams p)
     tmem_ld32(t_s + t_lane, s);
     tmem_ld32(t_s + t_lane + 32, s + 32);
     const int tok0 = j * kKeyTile;
-    float mx = -CUDART_INF_F;
+    if (tok0 + kKeyTile - 1 > pos) {  // the tile crosses this row's causal limit
 #pragma unroll
-    for (int c = 0; c < kKeyTile; ++c) {
-      const float v = neg ? -s[c] : s[c];
-      s[c] = (tok0 + c <= pos) ? v : -CUDART_INF_F;
-      mx = fmaxf(mx, s[c]);
+      for (int c = 0; c < kKeyTile; ++c)
+        if (tok0 + c > pos) s[c] = -CUDART_INF_F;
     }
+    // row max and sum as 8 independent partial chains, not one 64-deep chain
+    float mp[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) mp[k] = s[k];
+#pragma unroll
+    for (int c = 8; c < kKeyTile; ++c) mp[c & 7] = fmaxf(mp[c & 7], s[c]);
+    const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                           fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
     float alpha = 1.f;
     if (mx != -CUDART_INF_F &&
         (m_ref == -CUDART_INF_F || (mx - m_ref) * sl2 > kRescaleLog2)) {
@@ -303,12 +308,13 @@ __global__ void __launch_bounds__(kThreads) chunk_tc_kernel(const ChunkParams p)
       m_ref = mx;
     }
     const float mu = m_ref == -CUDART_INF_F ? 0.f : m_ref * sl2;
-    float sum = 0.f;
+    float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int c = 0; c < kKeyTile; ++c) {
       s[c] = ex2_approx(fmaf(s[c], sl2, -mu));  // masked: 2^-inf = 0
-      sum += s[c];
+      sp[c & 7] += s[c];
     }
+    const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
     l = fmaf(l, alpha, sum);
     // P row into the K-major swizzled tile, over the K tile when it fits: every
     // thread has seen the QK product complete (mbarrier above) before writing
