@@ -10,10 +10,14 @@
 //
 //   S [128 x 64] = Q [128 x D] . K_tile^T      tcgen05.mma -> tensor memory
 //   softmax      : thread r loads row r of S (tcgen05.ld), masks, takes the
-//                  running max and sum in fp32, and writes P (bf16/f16) in
-//                  the 128-byte-swizzled K-major layout over the K tile it
-//                  no longer needs
-//   O [128 x D] += P . V_tile                 tcgen05.mma, O stays in tensor memory
+//                  running max and sum in fp32, and writes row r of P
+//                  (bf16/f16 pairs) back over the first 32 columns of S
+//   O [128 x D] += P . V_tile                 tcgen05.mma with A (P) read from
+//                                             tensor memory; O stays there too
+//
+// P never touches shared memory, which then holds only Q and two K/V stages:
+// 49 KB at head_dim 64, so four CTAs share an SM (their 4 x 128 tensor-memory
+// columns fill it exactly).
 //
 // The running max used for the exponent is only moved when a row's max
 // grows by more than 2^8 (then O and l are rescaled, warp by warp, through
@@ -47,11 +51,9 @@ template <int D>
 struct TcShape {
   static constexpr int kQBytes = kRows * D * 2;         // Q: [kb][128 rows][128 B]
   static constexpr int kKVBytes = kKeyTile * D * 2;     // one K or V tile: [kb][64 rows][128 B]
-  static constexpr int kPBytes = kRows * kKeyTile * 2;  // P: [128 rows][128 B]
-  // P reuses the K buffer of its tile when that is large enough (D >= 128)
-  static constexpr bool kPInK = kKVBytes >= kPBytes;
-  static constexpr int kSmem = kQBytes + 4 * kKVBytes + (kPInK ? 0 : kPBytes) + 1024;
-  static constexpr int kTmemCols = (kKeyTile + D) <= 128 ? 128 : 256;  // S then O
+  static constexpr int kSmem = kQBytes + 4 * kKVBytes + 1024;
+  static constexpr int kTmemCols = (kKeyTile + D) <= 128 ? 128 : 256;  // S (P over it), then O
+  static constexpr int kMinBlocks = D <= 64 ? 4 : 2;                  // CTAs per SM
 };
 
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -79,6 +81,16 @@ __device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t da, uint64_t d
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(tmem_d),
       "l"(da), "l"(db), "r"(id), "r"(accumulate));
+}
+
+// The same product with A read from tensor memory (128 lanes x 8 columns of
+// packed 16-bit pairs per 16-wide K step) instead of a shared-memory descriptor.
+__device__ __forceinline__ void mma_f16_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t db,
+                                           uint32_t id, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(db), "r"(id), "r"(accumulate));
 }
 
 __device__ __forceinline__ void commit(uint32_t mbar) {
@@ -130,6 +142,18 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float *v) {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t *v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+      "r"(v[29]), "r"(v[30]), "r"(v[31]));
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 template <typename T> struct Pack2;
 template <> struct Pack2<__nv_bfloat16> {
   __device__ __forceinline__ static uint32_t run(float lo, float hi) {
@@ -150,7 +174,8 @@ __device__ __forceinline__ uint32_t sw_off(int row, int chunk, int rows) {
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kThreads) chunk_tc_kernel(const ChunkParams p) {
+__global__ void __launch_bounds__(kThreads, TcShape<D>::kMinBlocks)
+    chunk_tc_kernel(const ChunkParams p) {
   using S = TcShape<D>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ uint64_t mbar_s, mbar_o;
@@ -169,7 +194,6 @@ __global__ void __launch_bounds__(kThreads) chunk_tc_kernel(const ChunkParams p)
   unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   unsigned char *sq = smem;                     // Q
   unsigned char *skv = smem + S::kQBytes;       // K0, V0, K1, V1
-  unsigned char *sp_own = skv + 4 * S::kKVBytes;  // P when it cannot live in K
 
   if (tid == 0) {
     s_bad = 0;
@@ -268,7 +292,6 @@ __global__ void __launch_bounds__(kThreads) chunk_tc_kernel(const ChunkParams p)
     __syncthreads();
     const uint32_t ks_u = smem_u32(skv + (2 * stage) * S::kKVBytes);
     const uint32_t vs_u = ks_u + S::kKVBytes;
-    const uint32_t ps_u = S::kPInK ? ks_u : smem_u32(sp_own);
 
     // S = Q . K^T
     if (tid == 0) {
@@ -316,17 +339,13 @@ __global__ void __launch_bounds__(kThreads) chunk_tc_kernel(const ChunkParams p)
     }
     const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
     l = fmaf(l, alpha, sum);
-    // P row into the K-major swizzled tile, over the K tile when it fits: every
-    // thread has seen the QK product complete (mbarrier above) before writing
+    // P row over the first 32 columns of S (this thread's lane; its S values
+    // are already in registers): tokens 2c and 2c+1 share column c
+    {
+      uint32_t w[kKeyTile / 2];
 #pragma unroll
-    for (int c = 0; c < kKeyTile / 8; ++c) {
-      uint4 w;
-      w.x = Pack2<T>::run(s[8 * c + 0], s[8 * c + 1]);
-      w.y = Pack2<T>::run(s[8 * c + 2], s[8 * c + 3]);
-      w.z = Pack2<T>::run(s[8 * c + 4], s[8 * c + 5]);
-      w.w = Pack2<T>::run(s[8 * c + 6], s[8 * c + 7]);
-      *reinterpret_cast<uint4 *>((S::kPInK ? skv + (2 * stage) * S::kKVBytes : sp_own) +
-                                 tid * 128 + ((c ^ (tid & 7)) << 4)) = w;
+      for (int c = 0; c < kKeyTile / 2; ++c) w[c] = Pack2<T>::run(s[2 * c], s[2 * c + 1]);
+      tmem_st32u(t_s + t_lane, w);
     }
     // rescale this warp's O rows when any of them moved its reference max
     if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
@@ -339,17 +358,16 @@ __global__ void __launch_bounds__(kThreads) chunk_tc_kernel(const ChunkParams p)
         tmem_st32(t_o + t_lane + cb, o);
       }
     }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 
-    // O += P . V
+    // O += P . V (each 16-token step of P is 8 columns of tensor memory)
     if (tid == 0) {
 #pragma unroll
       for (int kk = 0; kk < kKeyTile / 16; ++kk) {
-        mma_f16(t_o, sw128_desc(ps_u + kk * 32, 16, 1024),
-                sw128_desc(vs_u + kk * 2048, kKeyTile * 128, 1024), id_pv, (j > 0 || kk > 0));
+        mma_f16_ta(t_o, t_s + kk * 8, sw128_desc(vs_u + kk * 2048, kKeyTile * 128, 1024), id_pv,
+                   (j > 0 || kk > 0));
       }
       commit(smem_u32(&mbar_o));
     }
