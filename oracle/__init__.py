@@ -17,4 +17,5 @@ from .paged_attention import (  # noqa: F401
     merge_partials,
     cache_append,
     paged_decode_chunk,
+    chunk_splitkv_partials,
 )

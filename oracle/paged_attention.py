@@ -42,6 +42,9 @@ Readings where the pages are silent (each one is listed in the design notes):
 * In a chunk of n_q queries, seq_len counts the history and the chunk, so
   past = seq_len - n_q; a query whose position is negative sees nothing and
   its output is 0.
+* A split of a chunked read covers the same fixed page run as a decode
+  split; query i's share of it stops at its causal limit past + i, so a
+  split that starts after that limit is empty for that query.
 
 Every pin of this oracle lives in tests/test_oracle_pins.py.
 """
@@ -227,3 +230,34 @@ def paged_decode_chunk(q, k_pool, v_pool, block_table, seq_lens, scale: float,
                 out[b, i, h], _ = attend(q[b, i, h], k_hist[:seen, g, :], v_hist[:seen, g, :],
                                          scale)
     return out
+
+
+def chunk_splitkv_partials(q, k_pool, v_pool, block_table, seq_lens, scale: float,
+                           page_size: int, pages_per_split: int, num_splits: int):
+    """Per-split partials of the chunked read: out [B, n_q, Hq, S, d], lse [B, n_q, Hq, S].
+
+    Split s covers the tokens of split_ranges(); query i of sequence b keeps
+    the part of it at or before its position past_b + i (the causal rule of
+    paged_decode_chunk) and reduces that part like a decode split.  Merging
+    the splits of a query with merge_partials gives paged_decode_chunk.
+    """
+    b_n, n_q, n_h, d = q.shape
+    n_kv = k_pool.shape[2]
+    part = np.zeros((b_n, n_q, n_h, num_splits, d), dtype=np.float64)
+    lse = np.full((b_n, n_q, n_h, num_splits), -np.inf, dtype=np.float64)
+    for b in range(b_n):
+        n = int(seq_lens[b])
+        past = n - n_q
+        k_hist, v_hist = gather_history(k_pool, v_pool, block_table[b], n, page_size)
+        ranges = split_ranges(n, page_size, pages_per_split, num_splits)
+        for i in range(n_q):
+            seen = max(0, past + i + 1)
+            for s, (lo, hi) in enumerate(ranges):
+                hi = min(hi, seen)
+                if hi <= lo:
+                    continue
+                for h in range(n_h):
+                    g = kv_head_of(h, n_h, n_kv)
+                    part[b, i, h, s], lse[b, i, h, s] = attend(
+                        q[b, i, h], k_hist[lo:hi, g, :], v_hist[lo:hi, g, :], scale)
+    return part, lse
