@@ -610,6 +610,43 @@ def chunk(pa, workloads, torch, dev, peak):
         del q, out
     del g
     torch.cuda.empty_cache()
+    return {"llama1b_h4096": rows, "longctx_h32768_split": chunk_longctx(pa, workloads, torch,
+                                                                          dev, peak, flush)}
+
+
+def chunk_longctx(pa, workloads, torch, dev, peak, flush):
+    """The chunked read on the long-context batch (8 x 32,768 tokens, head_dim 128): split
+    into 64-page runs (pa_decode_chunk_splitkv + pa_merge) against one pass."""
+    g = workloads.longctx(32768, device=str(dev))
+    lens = g.lens_list()
+    pps = g.pages_per_split
+    s = pa.pa_num_splits(g.max_blocks, pps)
+    rows = []
+    for n_q in (1, 4, 16):
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(9)
+        q = torch.randn((8, n_q, 32, 128), generator=gen, device=dev).to(torch.bfloat16)
+        out = torch.empty_like(q)
+        po = torch.empty((8, n_q, 32, s, 128), device=dev)
+        pl = torch.empty((8, n_q, 32, s), device=dev)
+
+        def fn():
+            pa.pa_decode_chunk_splitkv(po, pl, q, g.k_pool, g.v_pool, g.block_table, g.seq_lens,
+                                       g.scale, pps)
+            pa.pa_merge(out, po, pl)
+
+        med, _ = _time_launches(fn, torch, flush, iters=20)
+        one = lambda: pa.pa_decode_chunk(out, q, g.k_pool, g.v_pool, g.block_table, g.seq_lens,
+                                         g.scale)
+        med1, _ = _time_launches(one, torch, flush, iters=5)
+        rb = (read_bytes(lens, 32, 8, 128, 2, 16) + 2 * 8 * (n_q - 1) * 32 * 128 * 2 +
+              split_bytes(8 * n_q, 32, s, 128))
+        rows.append({"n_q": n_q, "splits": s, "us_split_plus_merge": 1e3 * med,
+                     "gbs": rb / (med * 1e-3) / 1e9, "frac_hbm": rb / (med * 1e-3) / 1e9 / peak,
+                     "us_single_pass": 1e3 * med1})
+        del q, out, po, pl
+    del g
+    torch.cuda.empty_cache()
     return rows
 
 

@@ -237,8 +237,8 @@ pa_status pa_decode_work(float *partial_out, float *partial_lse, const int32_t *
  * with chunk_len == seq_lens[b].  f16/bf16 only, head_dim 32, 48, 64, 96 or
  * 128 (otherwise PA_ERR_UNSUPPORTED); fp32 accumulation and softmax, the
  * probabilities rounded to the cache dtype for the P.V product.  Chunks of
- * at least 128 (query, head) rows per kv head at head_dim 64 or 128 run on
- * the tcgen05 tensor cores, smaller ones on mma.sync.
+ * at least 64 (query, head) rows per kv head at head_dim 64, or 128 rows at
+ * head_dim 128, run on the tcgen05 tensor cores; the rest on mma.sync.
  */
 pa_status pa_decode_chunk(void *out, const void *q, const void *k_pool,
                           const void *v_pool, const int32_t *block_table,
@@ -247,6 +247,37 @@ pa_status pa_decode_chunk(void *out, const void *q, const void *k_pool,
                           int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                           int32_t num_pages, float scale, pa_dtype dtype,
                           int32_t *dev_err, pa_stream_t stream);
+
+/*
+ * pa_decode_chunk_splitkv - the chunked read split into fixed page runs.
+ *
+ * "Three Attention Kernels", section "2. Split-KV flash-decoding", applied
+ * to pa_decode_chunk: split s of sequence b covers pages
+ * [s * pages_per_split, min((s+1) * pages_per_split, ceil(seq_lens[b] / block_size)))
+ * as in pa_decode_splitkv, and query i keeps the tokens of that run at or
+ * before its position past + i.  For every (b, i, h, s) it writes
+ *   partial_out[b][i][h][s][:] = softmax-weighted V over those tokens (fp32),
+ *   partial_lse[b][i][h][s]    = log(sum of exp(scale * q . k) over them),
+ * and 0 / -inf where a query sees no token of the run.  pa_merge with
+ * num_seqs * chunk_len as its sequence count combines them into the output
+ * of pa_decode_chunk.  This is the form for long histories, where one CTA
+ * per (sequence, kv head) would leave most of the GPU idle.
+ *
+ * partial_out [num_seqs][chunk_len][num_q_heads][max_splits][head_dim] and
+ * partial_lse [num_seqs][chunk_len][num_q_heads][max_splits] are
+ * caller-owned device float arrays (partial_out 16-byte aligned);
+ * max_splits >= pa_num_splits(max_blocks_per_seq, pages_per_split) and at
+ * most 65535; splits past a sequence's length are written as empty.  Other
+ * arguments, errors and supported shapes are those of pa_decode_chunk.
+ */
+pa_status pa_decode_chunk_splitkv(float *partial_out, float *partial_lse, const void *q,
+                                  const void *k_pool, const void *v_pool,
+                                  const int32_t *block_table, int32_t max_blocks_per_seq,
+                                  const int32_t *seq_lens, int32_t num_seqs, int32_t chunk_len,
+                                  int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                  int32_t block_size, int32_t num_pages, float scale,
+                                  int32_t pages_per_split, int32_t max_splits, pa_dtype dtype,
+                                  int32_t *dev_err, pa_stream_t stream);
 
 /* Size of the library-owned partials array behind pa_decode_splitkv_noalloc. */
 #define PA_NOALLOC_SCRATCH_BYTES (32u << 20)

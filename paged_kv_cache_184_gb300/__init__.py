@@ -7,7 +7,7 @@ CUDA stream.  All arithmetic runs in the library's CUDA kernels; there is
 no other implementation to fall back on, so a missing library raises.
 
 The names match the C ABI: pa_cache_append, pa_decode, pa_decode_splitkv,
-pa_merge, pa_decode_chunk, pa_plan_work, pa_decode_work,
+pa_merge, pa_decode_chunk, pa_decode_chunk_splitkv, pa_plan_work, pa_decode_work,
 pa_decode_splitkv_noalloc, pa_num_splits, pa_status_string, pa_version.
 """
 
@@ -28,7 +28,7 @@ PA_DEV_BAD_ITEM, PA_DEV_TIMEOUT = 5, 6
 
 EXPORTED = ("pa_status_string", "pa_version", "pa_num_splits", "pa_cache_append",
             "pa_decode", "pa_decode_splitkv", "pa_merge", "pa_decode_splitkv_noalloc",
-            "pa_decode_chunk", "pa_plan_work", "pa_decode_work")
+            "pa_decode_chunk", "pa_decode_chunk_splitkv", "pa_plan_work", "pa_decode_work")
 
 # bytes of the library-owned partials array behind pa_decode_splitkv_noalloc
 PA_NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -55,6 +55,8 @@ _SIGNATURES = {
                                       _i, _f, ctypes.c_int, _p, _p]),
     "pa_decode_chunk": (ctypes.c_int, [_p, _p, _p, _p, _p, _i, _p, _i, _i, _i, _i, _i, _i, _i, _f,
                                        ctypes.c_int, _p, _p]),
+    "pa_decode_chunk_splitkv": (ctypes.c_int, [_p, _p, _p, _p, _p, _p, _i, _p, _i, _i, _i, _i, _i,
+                                               _i, _i, _f, _i, _i, ctypes.c_int, _p, _p]),
     "pa_decode_splitkv_noalloc": (ctypes.c_int, [_p, _p, _p, _p, _p, _i, _p, _i, _i, _i, _i, _i,
                                                  _i, _f, _i, ctypes.c_int, _p, _p]),
 }
@@ -217,6 +219,35 @@ def pa_decode_chunk(out, q, k_pool, v_pool, block_table, seq_lens, scale: float,
     _check("pa_decode_chunk", st)
 
 
+def pa_decode_chunk_splitkv(partial_out, partial_lse, q, k_pool, v_pool, block_table, seq_lens,
+                            scale: float, pages_per_split: int, dev_err=None,
+                            stream=None) -> None:
+    """Per-split partials of the chunked read: [B, n_q, Hq, S, d] and [B, n_q, Hq, S] (float32).
+
+    pa_merge(out, partial_out, partial_lse) then gives pa_decode_chunk's out.
+    """
+    import torch
+    lib = load()
+    num_pages, block_size, hkv, d = k_pool.shape
+    b, nq, hq, dq = q.shape
+    max_splits = partial_lse.shape[-1]
+    if (dq != d or v_pool.shape != k_pool.shape or
+            partial_out.shape != (b, nq, hq, max_splits, d) or
+            partial_lse.shape != (b, nq, hq, max_splits)):
+        raise ValueError("pa_decode_chunk_splitkv: partial shapes must be [B,n_q,Hq,S,d] and "
+                         "[B,n_q,Hq,S]")
+    dt = q.dtype
+    st = lib.pa_decode_chunk_splitkv(
+        _ptr(partial_out, "partial_out", torch.float32),
+        _ptr(partial_lse, "partial_lse", torch.float32), _ptr(q, "q", dt),
+        _ptr(k_pool, "k_pool", dt), _ptr(v_pool, "v_pool", dt),
+        _ptr(block_table, "block_table", torch.int32), block_table.shape[1],
+        _ptr(seq_lens, "seq_lens", torch.int32), b, nq, hq, hkv, d, block_size, num_pages,
+        float(scale), int(pages_per_split), max_splits, _dtype_code(q),
+        _ptr(dev_err, "dev_err", torch.int32, allow_none=True), _stream(stream))
+    _check("pa_decode_chunk_splitkv", st)
+
+
 def pa_plan_work(seq_lens, num_kv_heads: int, block_size: int, target_ctas: int,
                  min_pages_per_item: int = 16):
     """Host work plan of a ragged batch: (items int32 [n, 4] on the CPU, max_slots).
@@ -264,12 +295,21 @@ def pa_decode_work(partial_out, partial_lse, items, q, k_pool, v_pool, block_tab
 
 
 def pa_merge(out, partial_out, partial_lse, stream=None) -> None:
-    """out[b, h] = sum_s w_s partial_out[b, h, s] / sum_s w_s, w_s = exp(lse_s - max lse)."""
+    """out[..., h] = sum_s w_s partial_out[..., h, s] / sum_s w_s, w_s = exp(lse_s - max lse).
+
+    partial_out [..., Hq, S, d], partial_lse [..., Hq, S], out [..., Hq, d]: the
+    leading axes ([B] for decode, [B, n_q] for a chunk) are one row axis.
+    """
     import torch
     lib = load()
-    b, hq, s, d = partial_out.shape
-    if out.shape != (b, hq, d) or partial_lse.shape != (b, hq, s):
+    if partial_out.dim() < 4:
+        raise ValueError("pa_merge: partial_out must be [..., Hq, S, d]")
+    *lead, hq, s, d = partial_out.shape
+    if (tuple(out.shape) != (*lead, hq, d) or tuple(partial_lse.shape) != (*lead, hq, s)):
         raise ValueError("pa_merge: inconsistent shapes")
+    b = 1
+    for x in lead:
+        b *= x
     st = lib.pa_merge(_ptr(out, "out"), _ptr(partial_out, "partial_out", torch.float32),
                       _ptr(partial_lse, "partial_lse", torch.float32), b, hq, s, d,
                       _dtype_code(out), _stream(stream))

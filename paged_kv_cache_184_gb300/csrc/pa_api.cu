@@ -278,6 +278,57 @@ pa_status pa_decode_chunk(void *out, const void *q, const void *k_pool, const vo
   return launched(pa::launch_chunk(p, dtype, s));
 }
 
+pa_status pa_decode_chunk_splitkv(float *partial_out, float *partial_lse, const void *q,
+                                  const void *k_pool, const void *v_pool,
+                                  const int32_t *block_table, int32_t max_blocks_per_seq,
+                                  const int32_t *seq_lens, int32_t num_seqs, int32_t chunk_len,
+                                  int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                  int32_t block_size, int32_t num_pages, float scale,
+                                  int32_t pages_per_split, int32_t max_splits, pa_dtype dtype,
+                                  int32_t *dev_err, pa_stream_t stream) {
+  if (chunk_len <= 0 || pages_per_split <= 0) return PA_ERR_INVALID_ARG;
+  pa_status st = check_read_shape(max_blocks_per_seq, num_seqs, num_q_heads, num_kv_heads,
+                                  head_dim, block_size, num_pages, scale, dtype);
+  if (st != PA_OK) return st;
+  if (!pa::chunk_supports(dtype, head_dim)) return PA_ERR_UNSUPPORTED;
+  const int32_t need = pa_num_splits(max_blocks_per_seq, pages_per_split);
+  if (max_splits < need) return PA_ERR_INVALID_ARG;
+  if (max_splits > 65535) return PA_ERR_UNSUPPORTED;  // the split is the grid's z index
+  const int64_t rows = static_cast<int64_t>(chunk_len) * (num_q_heads / num_kv_heads);
+  const int64_t ctas = (rows + pa::chunk_rows_per_cta() - 1) / pa::chunk_rows_per_cta();
+  if (ctas * num_kv_heads > INT32_MAX) return PA_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return PA_OK;
+  if (!partial_out || !partial_lse || !q || !k_pool || !v_pool || !block_table || !seq_lens)
+    return PA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(partial_out))
+    return PA_ERR_INVALID_ARG;
+  pa::ChunkParams p{};
+  p.q = q;
+  p.k_pool = k_pool;
+  p.v_pool = v_pool;
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.dev_err = dev_err;
+  p.partial_out = partial_out;
+  p.partial_lse = partial_lse;
+  p.pages_per_split = pages_per_split;
+  p.num_splits = max_splits;
+  p.num_seqs = num_seqs;
+  p.chunk_len = chunk_len;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.head_dim = head_dim;
+  p.group = num_q_heads / num_kv_heads;
+  p.max_blocks = max_blocks_per_seq;
+  p.block_size_log2 = log2_exact(block_size);
+  p.num_pages = num_pages;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (pa::chunk_tc_supports(dtype, head_dim, static_cast<int>(rows)))
+    return launched(pa::launch_chunk_tc(p, dtype, s));
+  return launched(pa::launch_chunk(p, dtype, s));
+}
+
 pa_status pa_merge(void *out, const float *partial_out, const float *partial_lse,
                    int32_t num_seqs, int32_t num_q_heads, int32_t max_splits, int32_t head_dim,
                    pa_dtype dtype, pa_stream_t stream) {

@@ -19,6 +19,12 @@
 // accumulators as the A fragments of the second product without touching
 // shared memory.  Keys past a row's position are masked to -inf; a query at
 // a negative position sees nothing and its output is 0.
+//
+// The split read ("Three Attention Kernels", section "2. Split-KV
+// flash-decoding", applied to the chunk) runs the same CTA over one fixed
+// page run of the sequence (blockIdx.z): each row keeps the part of the run
+// at or before its causal limit and writes its fp32 partial output and
+// log-sum-exp for pa_merge instead of the final row.
 #include <math_constants.h>
 
 #include "pa_common.cuh"
@@ -102,6 +108,8 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 4 : 1) chunk_kernel(const 
   const int g = blockIdx.x % hkv;
   const int rblk = blockIdx.x / hkv;
   const int b = blockIdx.y;
+  const int split = blockIdx.z;
+  const bool partial = p.partial_out != nullptr;
   const int bs_log2 = p.block_size_log2, bs_mask = (1 << bs_log2) - 1;
   const int rows_total = nq * G;
 
@@ -116,17 +124,26 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 4 : 1) chunk_kernel(const 
     len = 0;
   }
   const int past = len - nq;  // position of query 0 (may be negative)
+  // tokens [t_lo, t_hi) of this CTA: the whole sequence, or one split of it
+  int t_lo = 0, t_hi = len;
+  if (partial) {
+    const long long span = static_cast<long long>(p.pages_per_split) << bs_log2;
+    t_lo = static_cast<int>(min(static_cast<long long>(len), split * span));
+    t_hi = static_cast<int>(min(static_cast<long long>(len), (split + 1) * span));
+  }
 
   // rows of this warp and of this thread's two fragment rows
   const int row0 = rblk * kRowsPerCta + warp * 16;
   const int ra = row0 + r, rb = row0 + r + 8;
-  const int pos_a = past + ra / G;  // causal limit of row ra (inclusive)
-  const int pos_b = past + rb / G;
+  // last key of row ra (inclusive): its causal limit, or the end of the split
+  const int pos_a = min(past + ra / G, t_hi - 1);
+  const int pos_b = min(past + rb / G, t_hi - 1);
   // key range of the CTA and of the warp
   const int cta_last_row = min(rows_total - 1, rblk * kRowsPerCta + kRowsPerCta - 1);
-  const int kv_end = max(0, min(len, past + cta_last_row / G + 1));
+  const int kv_end = max(t_lo, min(t_hi, past + cta_last_row / G + 1));
   const int warp_last_row = min(rows_total - 1, row0 + 15);
-  const int warp_end = row0 < rows_total ? max(0, min(len, past + warp_last_row / G + 1)) : 0;
+  const int warp_end =
+      row0 < rows_total ? max(t_lo, min(t_hi, past + warp_last_row / G + 1)) : t_lo;
 
   // Q rows as A fragments
   uint32_t qa[S::kSteps][4];
@@ -152,8 +169,8 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 4 : 1) chunk_kernel(const 
       qa[ks][3] = vb ? __ldg(reinterpret_cast<const uint32_t *>(pb_ + d0 + 8)) ^ flip : 0u;
     }
   }
-  // smallest causal limit among this warp's rows: tiles ending at or below it need no mask
-  const int warp_min_pos = past + row0 / G;
+  // smallest key limit among this warp's rows: tiles ending at or below it need no mask
+  const int warp_min_pos = min(past + row0 / G, t_hi - 1);
 
   const int32_t *bt_row = p.block_table + static_cast<size_t>(b) * p.max_blocks;
   const T *kpool = static_cast<const T *>(p.k_pool);
@@ -164,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 4 : 1) chunk_kernel(const 
   auto load_tile = [&](int j, int stage) {
     unsigned char *ks = smem + stage * S::kStageBytes;
     unsigned char *vs = ks + S::kTileBytes;
-    const int tok0 = j * kKeyTile;
+    const int tok0 = t_lo + j * kKeyTile;
 #pragma unroll
     for (int q = tid; q < kKeyTile * S::kChunks; q += kThreads) {
       const int row = q / S::kChunks;
@@ -191,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 4 : 1) chunk_kernel(const 
     }
   };
 
-  const int ntiles = (kv_end + kKeyTile - 1) / kKeyTile;
+  const int ntiles = (kv_end - t_lo + kKeyTile - 1) / kKeyTile;
 #pragma unroll
   for (int s = 0; s < kStages - 1; ++s) {
     if (s < ntiles) load_tile(s, s);
@@ -216,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 4 : 1) chunk_kernel(const 
       if (nj < ntiles) load_tile(nj, nj % kStages);
       cp_async_commit();
     }
-    const int tok0 = j * kKeyTile;
+    const int tok0 = t_lo + j * kKeyTile;
     if (tok0 >= warp_end) continue;  // every row of this warp is past its limit
     const uint32_t ks_u = ring + (j % kStages) * S::kStageBytes;
     const uint32_t vs_u = ks_u + S::kTileBytes;
@@ -322,13 +339,27 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 4 : 1) chunk_kernel(const 
   __syncthreads();  // s_bad final
   const bool bad = bad_len || (s_bad != 0);
 
-  T *ob = static_cast<T *>(p.out);
-  auto store_row = [&](int row, float l, int e0) {
+  auto store_row = [&](int row, float l, float m, int e0) {
     if (row >= rows_total) return;
     const int i = row / G, h = row - (row / G) * G;
-    T *dst = ob + ((static_cast<size_t>(b) * nq + i) * p.num_q_heads +
-                   static_cast<size_t>(g) * G + h) * D;
-    const float inv = (bad || l == 0.f) ? 0.f : 1.f / l;
+    const size_t orow = (static_cast<size_t>(b) * nq + i) * p.num_q_heads +
+                        static_cast<size_t>(g) * G + h;
+    const bool empty = bad || l == 0.f;
+    const float inv = empty ? 0.f : 1.f / l;
+    if (partial) {
+      const size_t prow = orow * p.num_splits + split;
+      float *dst = p.partial_out + prow * D;
+#pragma unroll
+      for (int n = 0; n < S::kDTiles; ++n)
+        *reinterpret_cast<float2 *>(dst + n * 8 + 2 * c) =
+            make_float2(o[n][e0] * inv, o[n][e0 + 1] * inv);
+      // natural-log lse of the row's scores over this split
+      if (c == 0)
+        p.partial_lse[prow] =
+            empty ? -CUDART_INF_F : fmaf(m, sl2, log2f(l)) * 0.69314718055994531f;
+      return;
+    }
+    T *dst = static_cast<T *>(p.out) + orow * D;
 #pragma unroll
     for (int n = 0; n < S::kDTiles; ++n) {
       const int d = n * 8 + 2 * c;
@@ -336,8 +367,8 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 4 : 1) chunk_kernel(const 
       dst[d + 1] = cvt_out<T>(o[n][e0 + 1] * inv);
     }
   };
-  store_row(ra, l_a, 0);
-  store_row(rb, l_b, 2);
+  store_row(ra, l_a, m_a, 0);
+  store_row(rb, l_b, m_b, 2);
 }
 
 template <typename T, int D>
@@ -347,7 +378,7 @@ cudaError_t launch_d(const ChunkParams &p, cudaStream_t stream) {
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   const int rblocks = (p.chunk_len * p.group + kRowsPerCta - 1) / kRowsPerCta;
-  dim3 grid(rblocks * p.num_kv_heads, p.num_seqs);
+  dim3 grid(rblocks * p.num_kv_heads, p.num_seqs, p.partial_out ? p.num_splits : 1);
   return launch_pdl(kern, grid, dim3(kThreads), smem, stream, p);
 }
 

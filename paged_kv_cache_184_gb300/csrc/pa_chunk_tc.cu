@@ -31,6 +31,12 @@
 // mbarrier by tcgen05.commit, and every wait on it is bounded: on time-out
 // the kernel records PA_DEV_TIMEOUT, waits (bounded) no further, frees its
 // tensor memory and leaves.
+//
+// In the split read (partial_out set) blockIdx.z picks one fixed page run of
+// the sequence ("Three Attention Kernels", section "2. Split-KV
+// flash-decoding"); every row stops at the earlier of its causal limit and
+// the end of the run, and writes its fp32 partial output and log-sum-exp
+// for pa_merge.
 #include <math_constants.h>
 
 #include <type_traits>
@@ -189,6 +195,8 @@ __global__ void __launch_bounds__(kThreads, TcShape<D>::kMinBlocks)
   const int nblk = (rows_total + kRows - 1) / kRows;
   const int rblk = nblk - 1 - blockIdx.x / hkv;  // the longest causal ranges start first
   const int b = blockIdx.y;
+  const int split = blockIdx.z;
+  const bool partial = p.partial_out != nullptr;
   const int bs_log2 = p.block_size_log2, bs_mask = (1 << bs_log2) - 1;
 
   unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -214,12 +222,22 @@ __global__ void __launch_bounds__(kThreads, TcShape<D>::kMinBlocks)
   const bool bad_len = (len < 0) || (static_cast<long long>(len) > cap);
   if (bad_len) len = 0;
   const int past = len - nq;
+  // tokens [t_lo, t_hi) of this CTA: the whole sequence, or one split of it
+  int t_lo = 0, t_hi = len;
+  if (partial) {
+    const long long span = static_cast<long long>(p.pages_per_split) << bs_log2;
+    t_lo = static_cast<int>(min(static_cast<long long>(len), split * span));
+    t_hi = static_cast<int>(min(static_cast<long long>(len), (split + 1) * span));
+  }
   const int row = rblk * kRows + tid;  // this thread's row
   const bool row_ok = row < rows_total;
-  const int pos = past + row / G;      // its causal limit (inclusive)
+  const int pos = min(past + row / G, t_hi - 1);  // its last key (inclusive)
   const int last_row = min(rows_total - 1, rblk * kRows + kRows - 1);
-  const int kv_end = max(0, min(len, past + last_row / G + 1));
-  const int ntiles = (kv_end + kKeyTile - 1) / kKeyTile;
+  const int kv_end = max(t_lo, min(t_hi, past + last_row / G + 1));
+  const int ntiles = (kv_end - t_lo + kKeyTile - 1) / kKeyTile;
+  // a warp whose 32 rows are all past the chunk's last row skips the softmax
+  // (its rows of O are never stored)
+  const bool warp_live = rblk * kRows + warp * 32 < rows_total;
 
   // ---- Q rows into the swizzled K-major layout ----------------------------
   const T *qbase = static_cast<const T *>(p.q);
@@ -245,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, TcShape<D>::kMinBlocks)
     unsigned char *vs = ks + S::kKVBytes;
     for (int idx = tid; idx < kKeyTile * (D / 8); idx += kThreads) {
       const int tr = idx / (D / 8), c = idx - tr * (D / 8);
-      const int t = j * kKeyTile + tr;
+      const int t = t_lo + j * kKeyTile + tr;
       bool valid = t < kv_end;
       const T *ksrc = kpool, *vsrc = vpool;
       if (valid) {
@@ -306,58 +324,60 @@ __global__ void __launch_bounds__(kThreads, TcShape<D>::kMinBlocks)
     if (!wait_phase(smem_u32(&mbar_s), j & 1)) fail = true;
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 
-    // row `row` of S: mask, running max, probabilities
-    float s[kKeyTile];
-    tmem_ld32(t_s + t_lane, s);
-    tmem_ld32(t_s + t_lane + 32, s + 32);
-    const int tok0 = j * kKeyTile;
-    if (tok0 + kKeyTile - 1 > pos) {  // the tile crosses this row's causal limit
+    if (warp_live) {
+      // row `row` of S: mask, running max, probabilities
+      float s[kKeyTile];
+      tmem_ld32(t_s + t_lane, s);
+      tmem_ld32(t_s + t_lane + 32, s + 32);
+      const int tok0 = t_lo + j * kKeyTile;
+      if (tok0 + kKeyTile - 1 > pos) {  // the tile crosses this row's causal limit
 #pragma unroll
-      for (int c = 0; c < kKeyTile; ++c)
-        if (tok0 + c > pos) s[c] = -CUDART_INF_F;
-    }
-    // row max and sum as 8 independent partial chains, not one 64-deep chain
-    float mp[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) mp[k] = s[k];
-#pragma unroll
-    for (int c = 8; c < kKeyTile; ++c) mp[c & 7] = fmaxf(mp[c & 7], s[c]);
-    const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                           fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
-    float alpha = 1.f;
-    if (mx != -CUDART_INF_F &&
-        (m_ref == -CUDART_INF_F || (mx - m_ref) * sl2 > kRescaleLog2)) {
-      alpha = m_ref == -CUDART_INF_F ? 0.f : ex2_approx((m_ref - mx) * sl2);
-      m_ref = mx;
-    }
-    const float mu = m_ref == -CUDART_INF_F ? 0.f : m_ref * sl2;
-    float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int c = 0; c < kKeyTile; ++c) {
-      s[c] = ex2_approx(fmaf(s[c], sl2, -mu));  // masked: 2^-inf = 0
-      sp[c & 7] += s[c];
-    }
-    const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
-    l = fmaf(l, alpha, sum);
-    // P row over the first 32 columns of S (this thread's lane; its S values
-    // are already in registers): tokens 2c and 2c+1 share column c
-    {
-      uint32_t w[kKeyTile / 2];
-#pragma unroll
-      for (int c = 0; c < kKeyTile / 2; ++c) w[c] = Pack2<T>::run(s[2 * c], s[2 * c + 1]);
-      tmem_st32u(t_s + t_lane, w);
-    }
-    // rescale this warp's O rows when any of them moved its reference max
-    if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-      for (int cb = 0; cb < D; cb += 32) {
-        float o[32];
-        tmem_ld32(t_o + t_lane + cb, o);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] *= alpha;
-        tmem_st32(t_o + t_lane + cb, o);
+        for (int c = 0; c < kKeyTile; ++c)
+          if (tok0 + c > pos) s[c] = -CUDART_INF_F;
       }
-    }
+      // row max and sum as 8 independent partial chains, not one 64-deep chain
+      float mp[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mp[k] = s[k];
+#pragma unroll
+      for (int c = 8; c < kKeyTile; ++c) mp[c & 7] = fmaxf(mp[c & 7], s[c]);
+      const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+      float alpha = 1.f;
+      if (mx != -CUDART_INF_F &&
+          (m_ref == -CUDART_INF_F || (mx - m_ref) * sl2 > kRescaleLog2)) {
+        alpha = m_ref == -CUDART_INF_F ? 0.f : ex2_approx((m_ref - mx) * sl2);
+        m_ref = mx;
+      }
+      const float mu = m_ref == -CUDART_INF_F ? 0.f : m_ref * sl2;
+      float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < kKeyTile; ++c) {
+        s[c] = ex2_approx(fmaf(s[c], sl2, -mu));  // masked: 2^-inf = 0
+        sp[c & 7] += s[c];
+      }
+      const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+      l = fmaf(l, alpha, sum);
+      // P row over the first 32 columns of S (this thread's lane; its S values
+      // are already in registers): tokens 2c and 2c+1 share column c
+      {
+        uint32_t w[kKeyTile / 2];
+#pragma unroll
+        for (int c = 0; c < kKeyTile / 2; ++c) w[c] = Pack2<T>::run(s[2 * c], s[2 * c + 1]);
+        tmem_st32u(t_s + t_lane, w);
+      }
+      // rescale this warp's O rows when any of them moved its reference max
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+        for (int cb = 0; cb < D; cb += 32) {
+          float o[32];
+          tmem_ld32(t_o + t_lane + cb, o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] *= alpha;
+          tmem_st32(t_o + t_lane + cb, o);
+        }
+      }
+    }  // warp_live
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -386,12 +406,17 @@ __global__ void __launch_bounds__(kThreads, TcShape<D>::kMinBlocks)
   __syncthreads();
   const bool bad = bad_len || s_bad != 0 || fail;
   const bool have_o = ntiles > 0 && !fail;  // uniform over the CTA
-  T *dst = static_cast<T *>(p.out);
+  size_t orow = 0;
   if (row_ok) {
     const int i = row / G, h = row - (row / G) * G;
-    dst += ((static_cast<size_t>(b) * nq + i) * p.num_q_heads + static_cast<size_t>(g) * G + h) * D;
+    orow = (static_cast<size_t>(b) * nq + i) * p.num_q_heads + static_cast<size_t>(g) * G + h;
   }
-  const float inv = (bad || l == 0.f || !have_o) ? 0.f : 1.f / l;
+  const bool empty = bad || l == 0.f || !have_o;
+  const float inv = empty ? 0.f : 1.f / l;
+  const size_t prow = orow * p.num_splits + split;  // used in the split read only
+  if (partial && row_ok)  // natural-log lse of the row's scores over this split
+    p.partial_lse[prow] =
+        empty ? -CUDART_INF_F : fmaf(m_ref, sl2, log2f(l)) * 0.69314718055994531f;
 #pragma unroll
   for (int cb = 0; cb < D; cb += 32) {
     float o[32];
@@ -401,7 +426,14 @@ __global__ void __launch_bounds__(kThreads, TcShape<D>::kMinBlocks)
 #pragma unroll
       for (int e = 0; e < 32; ++e) o[e] = 0.f;
     }
-    if (row_ok) {
+    if (row_ok && partial) {
+      float *dst = p.partial_out + prow * D + cb;
+#pragma unroll
+      for (int e = 0; e < 32; e += 4)
+        *reinterpret_cast<float4 *>(dst + e) =
+            make_float4(o[e] * inv, o[e + 1] * inv, o[e + 2] * inv, o[e + 3] * inv);
+    } else if (row_ok) {
+      T *dst = static_cast<T *>(p.out) + orow * D + cb;
 #pragma unroll
       for (int e = 0; e < 32; e += 8) {
         uint4 w;
@@ -409,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, TcShape<D>::kMinBlocks)
         w.y = Pack2<T>::run(o[e + 2] * inv, o[e + 3] * inv);
         w.z = Pack2<T>::run(o[e + 4] * inv, o[e + 5] * inv);
         w.w = Pack2<T>::run(o[e + 6] * inv, o[e + 7] * inv);
-        *reinterpret_cast<uint4 *>(dst + cb + e) = w;
+        *reinterpret_cast<uint4 *>(dst + e) = w;
       }
     }
   }
@@ -428,7 +460,7 @@ cudaError_t launch_d(const ChunkParams &p, cudaStream_t stream) {
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   const int nblk = (p.chunk_len * p.group + kRows - 1) / kRows;
-  dim3 grid(nblk * p.num_kv_heads, p.num_seqs);
+  dim3 grid(nblk * p.num_kv_heads, p.num_seqs, p.partial_out ? p.num_splits : 1);
   return launch_pdl(kern, grid, dim3(kThreads), smem, stream, p);
 }
 
@@ -443,10 +475,13 @@ cudaError_t launch_t(const ChunkParams &p, cudaStream_t stream) {
 
 }  // namespace
 
+// At head_dim 64 this read measured faster than the mma.sync one from 64
+// rows per (sequence, kv head) on, even with half of the 128-row tile idle;
+// at head_dim 128 only from a full tile on.
 bool chunk_tc_supports(pa_dtype dtype, int head_dim, int rows) {
   if (dtype != PA_F16 && dtype != PA_BF16) return false;
   if (head_dim != 64 && head_dim != 128) return false;
-  return rows >= kRows;  // at least one full 128-row tile per (sequence, kv head)
+  return rows >= (head_dim == 64 ? kRows / 2 : kRows);
 }
 
 cudaError_t launch_chunk_tc(const ChunkParams &p, pa_dtype dtype, cudaStream_t stream) {

@@ -55,11 +55,16 @@ struct DecodeParams {
 
 // Arguments of the chunked multi-query read (pa_decode_chunk).
 struct ChunkParams {
-  void *out;                   // [B][chunk_len][Hq][D]
+  void *out;                   // [B][chunk_len][Hq][D] (one-pass read)
   const void *q;               // [B][chunk_len][Hq][D]
   const void *k_pool, *v_pool;
   const int32_t *block_table, *seq_lens;
   int32_t *dev_err;
+  // split read (partial_out non-null): blockIdx.z is the split, which covers
+  // pages [z * pages_per_split, (z + 1) * pages_per_split) of the sequence
+  float *partial_out;          // [B][chunk_len][Hq][num_splits][D]
+  float *partial_lse;          // [B][chunk_len][Hq][num_splits]
+  int32_t pages_per_split, num_splits;
   int32_t num_seqs, chunk_len, num_q_heads, num_kv_heads, head_dim, group;
   int32_t max_blocks, block_size_log2, num_pages;
   float scale_log2;

@@ -219,3 +219,25 @@ def test_work_validation(lib, kw, want):
                                   a["hkv"], a["d"], a["bs"], a["np_"], a["scale"], a["dt"],
                                   None, None)
     assert st == want
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(nq=0), pa.PA_ERR_INVALID_ARG),
+    (dict(pps=0), pa.PA_ERR_INVALID_ARG),
+    (dict(dt=pa.PA_F32), pa.PA_ERR_UNSUPPORTED),          # tensor-core read only
+    (dict(d=80), pa.PA_ERR_UNSUPPORTED),
+    (dict(ms=3), pa.PA_ERR_INVALID_ARG),                  # 4 pages, 1 per split: 4 needed
+    (dict(ms=70000), pa.PA_ERR_UNSUPPORTED),              # the split is the grid's z index
+    (dict(po=MISALIGNED), pa.PA_ERR_INVALID_ARG),
+    (dict(pl=None), pa.PA_ERR_INVALID_ARG),
+    (dict(b=0), pa.PA_OK),
+])
+def test_chunk_splitkv_validation(lib, kw, want):
+    a = dict(po=FAKE, pl=FAKE, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, mb=4, sl=FAKE, b=2, nq=8, hq=8,
+             hkv=2, d=64, bs=16, np_=32, scale=0.125, pps=1, ms=4, dt=pa.PA_BF16)
+    a.update(kw)
+    st = lib.raw().pa_decode_chunk_splitkv(
+        a["po"], a["pl"], a["q"], a["k"], a["v"], a["bt"], a["mb"], a["sl"], a["b"], a["nq"],
+        a["hq"], a["hkv"], a["d"], a["bs"], a["np_"], a["scale"], a["pps"], a["ms"], a["dt"],
+        None, None)
+    assert st == want

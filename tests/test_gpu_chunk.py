@@ -113,13 +113,13 @@ def test_any_finite_scale(lib, scale):
     assert_attn_close(out, _ref(base, q), base.dtype, f"scale {scale}")
 
 
-# ---------------------------------------------------------------- tcgen05 path (>= 128 rows)
+# ------------------------------------------- tcgen05 path (>= 64 rows at d 64, 128 at d 128)
 
 
 @pytest.mark.parametrize("dtype,hq,hkv,d,bs,n_q,lens", [
     ("bf16", 32, 8, 64, 16, 32, [32, 100, 700, 4096]),       # 128 rows: one tile
     ("bf16", 32, 8, 64, 16, 50, [60, 50, 333, 1000]),        # 200 rows: a partial second tile
-    ("bf16", 32, 8, 128, 16, 40, [40, 41, 500, 2049]),       # head_dim 128, P over the K tile
+    ("bf16", 32, 8, 128, 16, 40, [40, 41, 500, 2049]),       # head_dim 128
     ("f16", 32, 8, 128, 8, 64, [64, 65, 129, 900]),          # fp16, pages of 8
     ("bf16", 32, 4, 64, 32, 16, [16, 300, 777, 1500]),       # group 8
     ("bf16", 32, 2, 128, 16, 8, [8, 9, 250, 3000]),          # group 16
