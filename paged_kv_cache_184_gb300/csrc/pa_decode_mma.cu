@@ -51,6 +51,7 @@ namespace {
 constexpr int kWarps = PA_MMA_WARPS;
 constexpr int kThreads = kWarps * 32;
 constexpr int kTile = 16;  // tokens per tile (the mma M dimension)
+constexpr float kLazyLog2 = 8.f;  // the running max moves when a score passes it by 2^8
 
 template <typename T> struct MmaT;
 template <> struct MmaT<__nv_bfloat16> {
@@ -383,8 +384,15 @@ __global__ void __launch_bounds__(kThreads)
     if constexpr (MULTI) {
       while (cur < (warp + i * kWarps) / tiles_per_split) finalize(cur++);
     }
-    cp_async_wait<S::kStages - 2>();
-    __syncwarp();
+    // Tile i + kStages - 1 goes into the stage tile i - 1 left.  A 2-stage
+    // ring refills before waiting for tile i (two tiles in flight during the
+    // wait, not one); a 3-stage ring waits first, which measured faster.
+    if constexpr (S::kStages > 2) {
+      cp_async_wait<S::kStages - 2>();
+      __syncwarp();
+    } else {
+      __syncwarp();  // the reads of tile i - 1's stage are done
+    }
     {
       const int ni = i + S::kStages - 1;
       if (ni < my_tiles) {
@@ -392,6 +400,10 @@ __global__ void __launch_bounds__(kThreads)
         pid_next = fetch_pid(ni + 1);
       }
       cp_async_commit();
+    }
+    if constexpr (S::kStages <= 2) {
+      cp_async_wait<S::kStages - 1>();
+      __syncwarp();
     }
     const int stage = i % S::kStages;
     const uint32_t ks_u32 = ring_u32 + stage * S::kStageBytes;
@@ -419,7 +431,6 @@ __global__ void __launch_bounds__(kThreads)
     // online softmax over this tile, per head column
     const bool v0 = tok0 + r < t_end;
     const bool v1 = tok0 + r + 8 < t_end;
-    float alpha[NT][2];
     uint32_t pb[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -428,28 +439,44 @@ __global__ void __launch_bounds__(kThreads)
       float s2 = v1 ? sc[nt][2] * sl2 : -CUDART_INF_F;  // token r+8, head 2c
       float s3 = v1 ? sc[nt][3] * sl2 : -CUDART_INF_F;  // token r+8, head 2c+1
       float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+      // m is a reference max shared by O and l.  It moves only when a lane's
+      // score passes it by more than 2^kLazyLog2 (one vote, not a shuffle
+      // reduction and a rescale of O on every tile); between moves the
+      // exponents below stay under 2^kLazyLog2, and O / l is unchanged.
+      if (__any_sync(0xffffffffu, mx0 > m[nt][0] + kLazyLog2 || mx1 > m[nt][1] + kLazyLog2)) {
 #pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
+        // nothing accumulated yet under an infinite reference: O and l are 0
+        const float a0 = m[nt][0] == -CUDART_INF_F ? 0.f : ex2_approx(m[nt][0] - mn0);
+        const float a1 = m[nt][1] == -CUDART_INF_F ? 0.f : ex2_approx(m[nt][1] - mn1);
+        m[nt][0] = mn0;
+        m[nt][1] = mn1;
+        l[nt][0] *= a0;
+        l[nt][1] *= a1;
+#pragma unroll
+        for (int mt = 0; mt < S::kSteps; ++mt) {
+          o[mt][nt][0] *= a0;
+          o[mt][nt][1] *= a1;
+          o[mt][nt][2] *= a0;
+          o[mt][nt][3] *= a1;
+        }
       }
-      const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
-      const float mu0 = mn0 == -CUDART_INF_F ? 0.f : mn0;
-      const float mu1 = mn1 == -CUDART_INF_F ? 0.f : mn1;
-      alpha[nt][0] = exp2f(m[nt][0] - mu0);
-      alpha[nt][1] = exp2f(m[nt][1] - mu1);
-      m[nt][0] = mn0;
-      m[nt][1] = mn1;
-      const float p0 = exp2f(s0 - mu0), p1 = exp2f(s1 - mu1);
-      const float p2 = exp2f(s2 - mu0), p3 = exp2f(s3 - mu1);
-      l[nt][0] = fmaf(l[nt][0], alpha[nt][0], p0 + p2);
-      l[nt][1] = fmaf(l[nt][1], alpha[nt][1], p1 + p3);
+      const float mu0 = m[nt][0] == -CUDART_INF_F ? 0.f : m[nt][0];
+      const float mu1 = m[nt][1] == -CUDART_INF_F ? 0.f : m[nt][1];
+      const float p0 = ex2_approx(s0 - mu0), p1 = ex2_approx(s1 - mu1);  // masked: 2^-inf = 0
+      const float p2 = ex2_approx(s2 - mu0), p3 = ex2_approx(s3 - mu1);
+      l[nt][0] += p0 + p2;
+      l[nt][1] += p1 + p3;
       // P^T blocks (tokens 0-7 | 8-15) x heads, transposed into B fragments
       pb[nt][0] = movmatrix_trans(M::pack(p0, p1));
       pb[nt][1] = movmatrix_trans(M::pack(p2, p3));
     }
 
-    // O^T = alpha * O^T + V^T . P^T
+    // O^T += V^T . P^T
 #pragma unroll
     for (int mt = 0; mt < S::kSteps; ++mt) {
       // matrices of V^T: (d lo, tok 0-7), (d hi, tok 0-7), (d lo, tok 8-15), (d hi, tok 8-15)
@@ -459,13 +486,7 @@ __global__ void __launch_bounds__(kThreads)
       uint32_t a[4];
       ldsm_x4_trans(a, vs_u32 + tile_off<D, NT>(row, chunk));
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        o[mt][nt][0] *= alpha[nt][0];
-        o[mt][nt][1] *= alpha[nt][1];
-        o[mt][nt][2] *= alpha[nt][0];
-        o[mt][nt][3] *= alpha[nt][1];
-        M::mma(o[mt][nt], a, pb[nt]);
-      }
+      for (int nt = 0; nt < NT; ++nt) M::mma(o[mt][nt], a, pb[nt]);
     }
   }
   cp_async_wait_all();
