@@ -236,6 +236,17 @@ pa_status pa_decode_work(float *partial_out, float *partial_lse, const int32_t *
   return launched(pa::launch_decode_items(p, dtype, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// The chunk read for this many (query, head) rows per kv head: warp-specialized
+// tcgen05 for chunks of two full 128-row tiles or more, single-tile tcgen05 from
+// 64 (head_dim 64) or 128 (head_dim 128) rows, mma.sync below that.
+static cudaError_t launch_chunk_read(const pa::ChunkParams &p, pa_dtype dtype, int64_t rows,
+                                     cudaStream_t s) {
+  const int r = static_cast<int>(rows);
+  if (pa::chunk_tc_ws_supports(dtype, p.head_dim, r)) return pa::launch_chunk_tc_ws(p, dtype, s);
+  if (pa::chunk_tc_supports(dtype, p.head_dim, r)) return pa::launch_chunk_tc(p, dtype, s);
+  return pa::launch_chunk(p, dtype, s);
+}
+
 pa_status pa_decode_chunk(void *out, const void *q, const void *k_pool, const void *v_pool,
                           const int32_t *block_table, int32_t max_blocks_per_seq,
                           const int32_t *seq_lens, int32_t num_seqs, int32_t chunk_len,
@@ -273,9 +284,7 @@ pa_status pa_decode_chunk(void *out, const void *q, const void *k_pool, const vo
   p.num_pages = num_pages;
   p.scale_log2 = scale * 1.4426950408889634f;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (pa::chunk_tc_supports(dtype, head_dim, static_cast<int>(rows)))
-    return launched(pa::launch_chunk_tc(p, dtype, s));
-  return launched(pa::launch_chunk(p, dtype, s));
+  return launched(launch_chunk_read(p, dtype, rows, s));
 }
 
 pa_status pa_decode_chunk_splitkv(float *partial_out, float *partial_lse, const void *q,
@@ -324,9 +333,7 @@ pa_status pa_decode_chunk_splitkv(float *partial_out, float *partial_lse, const 
   p.num_pages = num_pages;
   p.scale_log2 = scale * 1.4426950408889634f;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (pa::chunk_tc_supports(dtype, head_dim, static_cast<int>(rows)))
-    return launched(pa::launch_chunk_tc(p, dtype, s));
-  return launched(pa::launch_chunk(p, dtype, s));
+  return launched(launch_chunk_read(p, dtype, rows, s));
 }
 
 pa_status pa_merge(void *out, const float *partial_out, const float *partial_lse,

@@ -39,18 +39,18 @@
 // for pa_merge.
 #include <math_constants.h>
 
-#include <type_traits>
-
 #include "pa_common.cuh"
 #include "pa_internal.h"
+#include "pa_tc.cuh"
 
 namespace pa {
 namespace {
 
+using namespace tc;
+
 constexpr int kRows = 128;      // rows per CTA (the MMA M), one per thread
 constexpr int kThreads = 128;
 constexpr int kKeyTile = 64;    // tokens per tile (the QK MMA N, the PV MMA K)
-constexpr uint32_t kSpinLimit = 1u << 26;
 constexpr float kRescaleLog2 = 8.f;  // move the reference max when it grows by more than 2^8
 
 template <int D>
@@ -61,123 +61,6 @@ struct TcShape {
   static constexpr int kTmemCols = (kKeyTile + D) <= 128 ? 128 : 256;  // S (P over it), then O
   static constexpr int kMinBlocks = D <= 64 ? 4 : 2;                  // CTAs per SM
 };
-
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = static_cast<uint64_t>((saddr >> 4) & 0x3FFF);
-  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFF) << 16;
-  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFF) << 32;
-  d |= static_cast<uint64_t>(1) << 46;  // descriptor version of this architecture
-  d |= static_cast<uint64_t>(2) << 61;  // 128-byte swizzle
-  return d;
-}
-
-// Instruction descriptor of kind::f16: fp32 accumulate, A/B element type,
-// A K-major, B K-major or MN-major, N and M.
-template <typename T>
-__host__ __device__ constexpr uint32_t idesc(int m, int n, bool b_mn_major, bool negate_a) {
-  const uint32_t ab = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
-  return (1u << 4) | (ab << 7) | (ab << 10) | ((negate_a ? 1u : 0u) << 13) |
-         ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(n >> 3) << 17) |
-         (static_cast<uint32_t>(m >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t id,
-                                        uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(tmem_d),
-      "l"(da), "l"(db), "r"(id), "r"(accumulate));
-}
-
-// The same product with A read from tensor memory (128 lanes x 8 columns of
-// packed 16-bit pairs per 16-wide K step) instead of a shared-memory descriptor.
-__device__ __forceinline__ void mma_f16_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t db,
-                                           uint32_t id, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(tmem_d),
-      "r"(tmem_a), "l"(db), "r"(id), "r"(accumulate));
-}
-
-__device__ __forceinline__ void commit(uint32_t mbar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   mbar)
-               : "memory");
-}
-
-// Wait for the given phase of an mbarrier; false after kSpinLimit polls.
-__device__ __forceinline__ bool wait_phase(uint32_t mbar, uint32_t phase) {
-  for (uint32_t it = 0; it < kSpinLimit; ++it) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}\n"
-        : "=r"(done)
-        : "r"(mbar), "r"(phase)
-        : "memory");
-    if (done) return true;
-  }
-  return false;
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-}
-
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float *v) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]),
-      "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]),
-      "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]),
-      "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]),
-      "f"(v[29]), "f"(v[30]), "f"(v[31]));
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t *v) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
-      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
-      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
-      "r"(v[29]), "r"(v[30]), "r"(v[31]));
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-template <typename T> struct Pack2;
-template <> struct Pack2<__nv_bfloat16> {
-  __device__ __forceinline__ static uint32_t run(float lo, float hi) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&v);
-  }
-};
-template <> struct Pack2<__half> {
-  __device__ __forceinline__ static uint32_t run(float lo, float hi) {
-    __half2 v = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&v);
-  }
-};
-
-// byte offset of 16-byte chunk `chunk` of row `row` in a [kb][rows][128 B] swizzled tile
-__device__ __forceinline__ uint32_t sw_off(int row, int chunk, int rows) {
-  return (chunk >> 3) * rows * 128 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
-}
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, TcShape<D>::kMinBlocks)

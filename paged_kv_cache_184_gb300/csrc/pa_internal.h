@@ -101,6 +101,10 @@ cudaError_t launch_chunk(const ChunkParams &p, pa_dtype dtype, cudaStream_t stre
 // f16/bf16, head_dim 64 or 128.
 bool chunk_tc_supports(pa_dtype dtype, int head_dim, int rows);
 cudaError_t launch_chunk_tc(const ChunkParams &p, pa_dtype dtype, cudaStream_t stream);
+
+// warp-specialized tcgen05 chunk read (pa_chunk_tc_ws.cu): two 128-row Q tiles per CTA
+bool chunk_tc_ws_supports(pa_dtype dtype, int head_dim, int rows);
+cudaError_t launch_chunk_tc_ws(const ChunkParams &p, pa_dtype dtype, cudaStream_t stream);
 cudaError_t launch_append(const AppendParams &p, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams &p, pa_dtype dtype, cudaStream_t stream);
 

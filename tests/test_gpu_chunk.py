@@ -187,3 +187,48 @@ def test_prefill_4096_sampled_rows(lib):
                 ref, _ = oracle.attend(host_f32(q[b, i, h]), k[:i + 1, h // 4], v[:i + 1, h // 4],
                                        base.scale)
                 assert_attn_close(out[b, i, h], ref, base.dtype, f"b{b} i{i} h{h}")
+
+
+# ------------------------------- warp-specialized tcgen05 path (>= 256 rows per kv head)
+
+
+@pytest.mark.parametrize("dtype,hq,hkv,d,bs,n_q,lens", [
+    ("bf16", 32, 8, 64, 16, 64, [64, 100, 700, 1000]),       # 256 rows: one CTA, two Q tiles
+    ("bf16", 32, 8, 64, 16, 100, [100, 130, 640, 2000]),     # 400 rows: second CTA's tile 1 partial
+    ("bf16", 32, 8, 128, 16, 80, [80, 81, 333, 1500]),       # 320 rows: second CTA's tile 1 empty
+    ("f16", 32, 8, 64, 8, 72, [72, 73, 200, 900]),           # fp16, pages of 8
+    ("bf16", 32, 2, 128, 16, 16, [16, 17, 300, 2500]),       # group 16
+    ("f16", 16, 4, 64, 16, 96, [30, 96, 200, 700]),          # queries at negative positions
+    ("bf16", 32, 8, 64, 32, 128, [128, 129, 1024, 4096]),    # 512 rows, pages of 32
+])
+def test_warp_specialized_chunks(lib, dtype, hq, hkv, d, bs, n_q, lens):
+    pages = sum(-(-n // bs) for n in lens) + 5
+    base = workloads.make_batch("ws", 46, dtype, lens, hq, hkv, d, bs, pages)
+    assert n_q * (hq // hkv) >= 256
+    q = _chunk_batch(base, n_q)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = _run(lib, base, q, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_attn_close(out, _ref(base, q), base.dtype)
+
+
+@pytest.mark.parametrize("scale", [-0.09, 0.0, 0.6])
+def test_warp_specialized_any_finite_scale(lib, scale):
+    base = workloads.make_batch("wss", 47, "bf16", [64, 300, 90], 32, 8, 64, 16, 40)
+    base.scale = scale
+    q = _chunk_batch(base, 64)
+    out = _run(lib, base, q)
+    assert_attn_close(out, _ref(base, q), base.dtype, f"scale {scale}")
+
+
+def test_warp_specialized_bad_page_is_reported_and_zeroed(lib):
+    base = workloads.make_batch("wsbad", 48, "bf16", [256, 300, 500], 32, 8, 128, 16, 80)
+    base.block_table[2, 5] = -3
+    q = _chunk_batch(base, 64)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = _run(lib, base, q, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 1
+    assert torch.all(out[2] == 0)
+    assert_attn_close(out[:2], _ref(base, q, [0, 1]), base.dtype)

@@ -74,6 +74,8 @@ def _check_partials(po, pl, ref_po, ref_pl, dtype, what=""):
     ("f16", 32, 8, 128, 8, 32, [32, 33, 129, 1000], 16),     # fp16, pages of 8
     ("bf16", 32, 2, 128, 16, 8, [8, 9, 250, 3000], 7),       # group 16: 128 rows
     ("bf16", 16, 4, 64, 16, 48, [20, 48, 130, 640], 1),      # queries at negative positions
+    ("bf16", 32, 8, 64, 16, 80, [80, 90, 700, 1300], 3),     # 320 rows: warp-specialized
+    ("f16", 32, 8, 128, 16, 64, [64, 200, 900, 1100], 8),    # 256 rows, head_dim 128
 ])
 def test_partials_and_merge(lib, dtype, hq, hkv, d, bs, n_q, lens, pps):
     pages = sum(-(-n // bs) for n in lens) + 5
