@@ -210,22 +210,14 @@ __global__ void __launch_bounds__(kThreads, TcShape<D>::kMinBlocks)
     if (warp_live) {
       // row `row` of S: mask, running max, probabilities
       float s[kKeyTile];
-      tmem_ld32(t_s + t_lane, s);
-      tmem_ld32(t_s + t_lane + 32, s + 32);
+      tmem_ld64(t_s + t_lane, s);
       const int tok0 = t_lo + j * kKeyTile;
       if (tok0 + kKeyTile - 1 > pos) {  // the tile crosses this row's causal limit
 #pragma unroll
         for (int c = 0; c < kKeyTile; ++c)
           if (tok0 + c > pos) s[c] = -CUDART_INF_F;
       }
-      // row max and sum as 8 independent partial chains, not one 64-deep chain
-      float mp[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mp[k] = s[k];
-#pragma unroll
-      for (int c = 8; c < kKeyTile; ++c) mp[c & 7] = fmaxf(mp[c & 7], s[c]);
-      const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+      const float mx = row_max64(s);
       float alpha = 1.f;
       if (mx != -CUDART_INF_F &&
           (m_ref == -CUDART_INF_F || (mx - m_ref) * sl2 > kRescaleLog2)) {
@@ -233,13 +225,7 @@ __global__ void __launch_bounds__(kThreads, TcShape<D>::kMinBlocks)
         m_ref = mx;
       }
       const float mu = m_ref == -CUDART_INF_F ? 0.f : m_ref * sl2;
-      float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int c = 0; c < kKeyTile; ++c) {
-        s[c] = ex2_approx(fmaf(s[c], sl2, -mu));  // masked: 2^-inf = 0
-        sp[c & 7] += s[c];
-      }
-      const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+      const float sum = row_exp64(s, sl2, mu);  // masked: 2^-inf = 0
       l = fmaf(l, alpha, sum);
       // P row over the first 32 columns of S (this thread's lane; its S values
       // are already in registers): tokens 2c and 2c+1 share column c

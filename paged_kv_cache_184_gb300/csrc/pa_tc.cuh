@@ -10,6 +10,8 @@
 #include <cstdint>
 #include <type_traits>
 
+#include "pa_common.cuh"  // ex2_approx
+
 namespace pa {
 namespace tc {
 
@@ -91,6 +93,27 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+// 64 consecutive columns of this warp's 32 lanes: both loads in flight, one wait
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float *v) {
+  uint32_t r[64];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t *q = r + 32 * h;
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3]), "=r"(q[4]), "=r"(q[5]), "=r"(q[6]),
+          "=r"(q[7]), "=r"(q[8]), "=r"(q[9]), "=r"(q[10]), "=r"(q[11]), "=r"(q[12]), "=r"(q[13]),
+          "=r"(q[14]), "=r"(q[15]), "=r"(q[16]), "=r"(q[17]), "=r"(q[18]), "=r"(q[19]),
+          "=r"(q[20]), "=r"(q[21]), "=r"(q[22]), "=r"(q[23]), "=r"(q[24]), "=r"(q[25]),
+          "=r"(q[26]), "=r"(q[27]), "=r"(q[28]), "=r"(q[29]), "=r"(q[30]), "=r"(q[31])
+        : "r"(taddr + 32 * h));
+  }
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 64; ++j) v[j] = __uint_as_float(r[j]);
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float *v) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
@@ -132,6 +155,63 @@ template <> struct Pack2<__half> {
 // byte offset of 16-byte chunk `chunk` of row `row` in a [kb][rows][128 B] swizzled tile
 __device__ __forceinline__ uint32_t sw_off(int row, int chunk, int rows) {
   return (chunk >> 3) * rows * 128 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
+}
+
+// ---- per-row softmax pieces on 64 scores (one row per thread) -------------
+// Paired fp32 arithmetic (f32x2) and the three-input max halve the issue
+// slots of the row max, the exponent arguments and the row sum; the
+// exponentials themselves stay one ex2.approx per score.
+
+__device__ __forceinline__ uint64_t pack_f2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+__device__ __forceinline__ void unpack_f2(uint64_t v, float &a, float &b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// max of s[0..63] (-inf when every score is masked)
+__device__ __forceinline__ float row_max64(const float *s) {
+  float r[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float m = max3(s[i], s[i + 8], s[i + 16]);
+    m = max3(m, s[i + 24], s[i + 32]);
+    m = max3(m, s[i + 40], s[i + 48]);
+    r[i] = fmaxf(m, s[i + 56]);
+  }
+  return max3(max3(r[0], r[1], r[2]), max3(r[3], r[4], r[5]), fmaxf(r[6], r[7]));
+}
+
+// s[c] <- 2^(s[c] * sl2 - mu) in place (a masked -inf gives 0); returns the sum
+__device__ __forceinline__ float row_exp64(float *s, float sl2, float mu) {
+  const uint64_t scale = pack_f2(sl2, sl2), shift = pack_f2(-mu, -mu);
+  uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    uint64_t x;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(x) : "l"(pack_f2(s[2 * c], s[2 * c + 1])),
+        "l"(scale), "l"(shift));
+    float a, b;
+    unpack_f2(x, a, b);
+    a = ex2_approx(a);
+    b = ex2_approx(b);
+    s[2 * c] = a;
+    s[2 * c + 1] = b;
+    asm("add.rn.f32x2 %0, %0, %1;" : "+l"(acc[c & 3]) : "l"(pack_f2(a, b)));
+  }
+  float t[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) unpack_f2(acc[i], t[2 * i], t[2 * i + 1]);
+  return ((t[0] + t[1]) + (t[2] + t[3])) + ((t[4] + t[5]) + (t[6] + t[7]));
 }
 
 }  // namespace tc
