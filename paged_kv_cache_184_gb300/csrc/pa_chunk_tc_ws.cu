@@ -104,6 +104,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ uint64_t bar_full[kStages], bar_empty[kStages];
   __shared__ uint64_t bar_s[kQTiles][2], bar_p[kQTiles][2], bar_o[kQTiles][2];
+  __shared__ uint64_t bar_turn[kQTiles];  // softmax groups take turns at the exponentials
   __shared__ uint32_t tmem_base;
   __shared__ int s_bad, s_fail;
 
@@ -138,6 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar_p[k][1], kQRows / 32);
       mbar_init(&bar_o[k][0], 1);
       mbar_init(&bar_o[k][1], 1);
+      mbar_init(&bar_turn[k], kQRows / 32);
     }
   }
   if (warp == kAllocWarp) {
@@ -395,15 +397,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------- softmax warps
     const int k = k_sm;
     const int pos = min(past + row / G, t_hi - 1);  // this row's last key (inclusive)
+    // At head_dim 128 the two groups take turns at the row max and
+    // exponentials of the tiles both Q tiles read (group 0 first), so each
+    // runs them with the exp unit of its SMSP to itself while the other loads
+    // S or stores P (at head_dim 64, with half the MMA time per tile to
+    // overlap, taking turns measured slower).  Group k
+    // waits on bar_turn[k]: group 0 for group 1's tile j - 1, group 1 for
+    // group 0's tile j.  Either barrier's next completion needs its waiter's
+    // own progress, so a parity wait never sees two completions.
+    const int n_pair = (nt[0] > 0 && nt[1] > 0) ? min(nt[0], nt[1]) : 0;
     for (int j = 0; j < my_nt; ++j) {
       if (!wait_phase(smem_u32(&bar_s[k][j & 1]), (j >> 1) & 1)) {
         fail = true;
         break;
       }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const uint32_t t_s = t_s0 + (j & 1) * kKeyTile;
+      float s[kKeyTile];
       if (warp_live) {
-        const uint32_t t_s = t_s0 + (j & 1) * kKeyTile;
-        float s[kKeyTile];
         tmem_ld64(t_s, s);
         const int tok0 = t_lo + j * kKeyTile;
         if (tok0 + kKeyTile - 1 > pos) {  // the tile crosses this row's last key
@@ -411,8 +422,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < kKeyTile; ++c)
             if (tok0 + c > pos) s[c] = -CUDART_INF_F;
         }
+      }
+      const bool turns = D > 64 && j < n_pair;
+      if (turns && (k == 1 || j > 0) &&
+          !wait_phase(smem_u32(&bar_turn[k]), (k == 0 ? j - 1 : j) & 1))
+        fail = true;
+      float alpha = 1.f;
+      if (warp_live && !fail) {
         const float mx = row_max64(s);
-        float alpha = 1.f;
         if (mx != -CUDART_INF_F &&
             (m_ref == -CUDART_INF_F || (mx - m_ref) * sl2 > kRescaleLog2)) {
           alpha = m_ref == -CUDART_INF_F ? 0.f : ex2_approx((m_ref - mx) * sl2);
@@ -421,6 +438,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float mu = m_ref == -CUDART_INF_F ? 0.f : m_ref * sl2;
         const float sum = row_exp64(s, sl2, mu);  // masked: 2^-inf = 0
         l = fmaf(l, alpha, sum);
+      }
+      if (turns) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_turn[1 - k]);
+      }
+      if (warp_live && !__any_sync(0xffffffffu, fail)) {
         {
           uint32_t w[kKeyTile / 2];
 #pragma unroll

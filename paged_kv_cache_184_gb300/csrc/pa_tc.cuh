@@ -63,11 +63,13 @@ __device__ __forceinline__ void commit(uint32_t mbar) {
 }
 
 // Wait for the given phase of an mbarrier; false after kSpinLimit polls.
+// Each poll may suspend the thread for at most 20 ns (the explicit hint
+// measured a few per cent faster than the default limit).
 __device__ __forceinline__ bool wait_phase(uint32_t mbar, uint32_t phase) {
   for (uint32_t it = 0; it < kSpinLimit; ++it) {
     uint32_t done;
     asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 20;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}\n"
         : "=r"(done)
         : "r"(mbar), "r"(phase)
