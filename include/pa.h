@@ -238,7 +238,10 @@ pa_status pa_decode_work(float *partial_out, float *partial_lse, const int32_t *
  * 128 (otherwise PA_ERR_UNSUPPORTED); fp32 accumulation and softmax, the
  * probabilities rounded to the cache dtype for the P.V product.  Chunks of
  * at least 64 (query, head) rows per kv head at head_dim 64, or 128 rows at
- * head_dim 128, run on the tcgen05 tensor cores; the rest on mma.sync.
+ * head_dim 128, run on the tcgen05 tensor cores (warp-specialized from 256
+ * rows); chunks of one query, or of up to 16 (query, head) columns per kv
+ * head at head_dim 64 (8 at head_dim 128), on the single-query read's kernel
+ * with a causal limit per column; the rest on the mma.sync chunk kernel.
  */
 pa_status pa_decode_chunk(void *out, const void *q, const void *k_pool,
                           const void *v_pool, const int32_t *block_table,

@@ -80,6 +80,8 @@ pa::DecodeParams make_params(const void *q, const void *k_pool, const void *v_po
   p.block_size_log2 = log2_exact(block_size);
   p.num_pages = num_pages;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.chunk_len = 1;
+  p.head_group = p.group;
   return p;
 }
 
@@ -265,6 +267,21 @@ pa_status pa_decode_chunk(void *out, const void *q, const void *k_pool, const vo
   if (!out || !q || !k_pool || !v_pool || !block_table || !seq_lens) return PA_ERR_INVALID_ARG;
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool))
     return PA_ERR_INVALID_ARG;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int group = num_q_heads / num_kv_heads;
+  // one query per sequence is the single-query read; up to 16 (query, head)
+  // columns per kv head run on its tensor-core kernel with per-column limits
+  if (chunk_len == 1 || pa::mma_chunk_supports(dtype, head_dim, chunk_len * group)) {
+    pa::DecodeParams dp = make_params(q, k_pool, v_pool, block_table, max_blocks_per_seq,
+                                      seq_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                      block_size, num_pages, scale, dev_err);
+    dp.out = out;
+    dp.pages_per_split = 0;
+    dp.num_splits = 1;
+    dp.chunk_len = chunk_len;
+    dp.group = chunk_len * group;
+    return launched(launch_read(dp, dtype, s));
+  }
   pa::ChunkParams p{};
   p.out = out;
   p.q = q;
@@ -283,7 +300,6 @@ pa_status pa_decode_chunk(void *out, const void *q, const void *k_pool, const vo
   p.block_size_log2 = log2_exact(block_size);
   p.num_pages = num_pages;
   p.scale_log2 = scale * 1.4426950408889634f;
-  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   return launched(launch_chunk_read(p, dtype, rows, s));
 }
 
@@ -311,6 +327,20 @@ pa_status pa_decode_chunk_splitkv(float *partial_out, float *partial_lse, const 
     return PA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(partial_out))
     return PA_ERR_INVALID_ARG;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int group = num_q_heads / num_kv_heads;
+  if (chunk_len == 1 || pa::mma_chunk_supports(dtype, head_dim, chunk_len * group)) {
+    pa::DecodeParams dp = make_params(q, k_pool, v_pool, block_table, max_blocks_per_seq,
+                                      seq_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                      block_size, num_pages, scale, dev_err);
+    dp.partial_out = partial_out;
+    dp.partial_lse = partial_lse;
+    dp.pages_per_split = pages_per_split;
+    dp.num_splits = max_splits;
+    dp.chunk_len = chunk_len;
+    dp.group = chunk_len * group;
+    return launched(launch_read(dp, dtype, s));
+  }
   pa::ChunkParams p{};
   p.q = q;
   p.k_pool = k_pool;
@@ -332,7 +362,6 @@ pa_status pa_decode_chunk_splitkv(float *partial_out, float *partial_lse, const 
   p.block_size_log2 = log2_exact(block_size);
   p.num_pages = num_pages;
   p.scale_log2 = scale * 1.4426950408889634f;
-  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   return launched(launch_chunk_read(p, dtype, rows, s));
 }
 

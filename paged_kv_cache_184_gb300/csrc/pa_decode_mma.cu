@@ -122,7 +122,9 @@ __device__ __forceinline__ uint32_t tile_off(int row, int chunk) {
   return row * Shape<D, NT>::kPitch + ((chunk ^ (row & 7)) << 4);
 }
 
-template <typename T, int D, int NT, bool MULTI, bool ITEMS>
+// CHUNK: the columns are (query, head) pairs of a chunk (see DecodeParams),
+// each with its own causal limit; otherwise they are the group's heads.
+template <typename T, int D, int NT, bool MULTI, bool ITEMS, bool CHUNK>
 __global__ void __launch_bounds__(kThreads)
     decode_mma_kernel(const DecodeParams p) {
   using S = Shape<D, NT>;
@@ -138,7 +140,18 @@ __global__ void __launch_bounds__(kThreads)
 
   const int hkv = p.num_kv_heads;
   const int g = blockIdx.x % hkv;
-  const int G = p.group;
+  const int G = p.group;  // columns: the group's heads, or a chunk's (query, head) pairs
+  // row of column h in q / out (and, times the split count, in the partials)
+  auto col_row = [&](int bb, int h) -> size_t {
+    if constexpr (CHUNK) {
+      const int hg = p.head_group;
+      const int i = h / hg;
+      return (static_cast<size_t>(bb) * p.chunk_len + i) * p.num_q_heads +
+             static_cast<size_t>(g) * hg + (h - i * hg);
+    } else {
+      return static_cast<size_t>(bb) * p.num_q_heads + static_cast<size_t>(g) * G + h;
+    }
+  };
   const int bs_log2 = p.block_size_log2;
   const int bs_mask = (1 << bs_log2) - 1;
   const long long cap = static_cast<long long>(p.max_blocks) << bs_log2;
@@ -200,10 +213,13 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int h = nt * 8 + r;
+      // a chunk's column h sits in its own query's row
+      const T *hrow = CHUNK ? static_cast<const T *>(p.q) + col_row(b, h < G ? h : 0) * D
+                            : qrow + h * D;
 #pragma unroll
       for (int ks = 0; ks < S::kSteps; ++ks) {
         if (h < G) {
-          const T *src = qrow + h * D + ks * 16 + 2 * c;
+          const T *src = hrow + ks * 16 + 2 * c;
           qb[nt][ks][0] = __ldg(reinterpret_cast<const uint32_t *>(src));
           qb[nt][ks][1] = __ldg(reinterpret_cast<const uint32_t *>(src + 8));
         } else {
@@ -222,6 +238,16 @@ __global__ void __launch_bounds__(kThreads)
   }
   const int t_begin = static_cast<int>(min(static_cast<long long>(len), lo));
   const int t_end = static_cast<int>(min(static_cast<long long>(len), lo + nsplit * span));
+  // CHUNK: last key of this lane's columns 2c, 2c+1 of every n-tile (query i
+  // of the chunk sits at len - chunk_len + i)
+  int lim[NT][2];
+  if constexpr (CHUNK) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+        lim[nt][e] = len - p.chunk_len + (nt * 8 + 2 * c + e) / p.head_group;
+  }
   // tiles per split (a CTA covers several splits only when a split is whole tiles)
   const int tiles_per_split = MULTI ? static_cast<int>(span / kTile) : 0x7fffffff;
 
@@ -357,7 +383,7 @@ __global__ void __launch_bounds__(kThreads)
       }
       const bool empty = bad || (Mx == -CUDART_INF_F);
       const float res = empty ? 0.f : O / L;
-      const size_t qh = static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(g) * G + h;
+      const size_t qh = col_row(b, h);
       if (is_split) {
         const size_t row = qh * p.num_splits + s0 + srel;
         p.partial_out[row * D + d] = res;
@@ -434,10 +460,17 @@ __global__ void __launch_bounds__(kThreads)
     uint32_t pb[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      float s0 = v0 ? sc[nt][0] * sl2 : -CUDART_INF_F;  // token r,   head 2c
-      float s1 = v0 ? sc[nt][1] * sl2 : -CUDART_INF_F;  // token r,   head 2c+1
-      float s2 = v1 ? sc[nt][2] * sl2 : -CUDART_INF_F;  // token r+8, head 2c
-      float s3 = v1 ? sc[nt][3] * sl2 : -CUDART_INF_F;  // token r+8, head 2c+1
+      bool u0 = v0, u1 = v0, u2 = v1, u3 = v1;
+      if constexpr (CHUNK) {  // and not past the column's query
+        u0 = u0 && tok0 + r <= lim[nt][0];
+        u1 = u1 && tok0 + r <= lim[nt][1];
+        u2 = u2 && tok0 + r + 8 <= lim[nt][0];
+        u3 = u3 && tok0 + r + 8 <= lim[nt][1];
+      }
+      float s0 = u0 ? sc[nt][0] * sl2 : -CUDART_INF_F;  // token r,   head 2c
+      float s1 = u1 ? sc[nt][1] * sl2 : -CUDART_INF_F;  // token r,   head 2c+1
+      float s2 = u2 ? sc[nt][2] * sl2 : -CUDART_INF_F;  // token r+8, head 2c
+      float s3 = u3 ? sc[nt][3] * sl2 : -CUDART_INF_F;  // token r+8, head 2c+1
       float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
       // m is a reference max shared by O and l.  It moves only when a lane's
       // score passes it by more than 2^kLazyLog2 (one vote, not a shuffle
@@ -548,7 +581,7 @@ __global__ void __launch_bounds__(kThreads)
       }
       const bool empty = bad || (Mx == -CUDART_INF_F);
       const float res = empty ? 0.f : O / L;
-      const size_t qh = static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(g) * G + h;
+      const size_t qh = col_row(b, h);
       if (is_split) {
         const size_t row = qh * p.num_splits + s0;
         p.partial_out[row * D + d] = res;
@@ -561,11 +594,11 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-template <typename T, int D, int NT>
+template <typename T, int D, int NT, bool CHUNK>
 cudaError_t launch_shape(DecodeParams p, cudaStream_t stream) {
   using S = Shape<D, NT>;
-  auto kern = decode_mma_kernel<T, D, NT, false, false>;
-  auto kern_multi = decode_mma_kernel<T, D, NT, true, false>;
+  auto kern = decode_mma_kernel<T, D, NT, false, false, CHUNK>;
+  auto kern_multi = decode_mma_kernel<T, D, NT, true, false, CHUNK>;
   p.splits_per_cta = 1;
   p.comb_heads = S::kHeads;
   int smem = S::kSmemBytes;
@@ -608,7 +641,7 @@ cudaError_t launch_shape(DecodeParams p, cudaStream_t stream) {
 template <typename T, int D, int NT>
 cudaError_t launch_items_shape(const DecodeParams &p, cudaStream_t stream) {
   using S = Shape<D, NT>;
-  auto kern = decode_mma_kernel<T, D, NT, false, true>;
+  auto kern = decode_mma_kernel<T, D, NT, false, true, false>;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
   if (err != cudaSuccess) return err;
@@ -622,8 +655,15 @@ cudaError_t launch_d(const DecodeParams &p, cudaStream_t stream) {
     if (p.group <= 8) return launch_items_shape<T, D, 1>(p, stream);
     return launch_items_shape<T, D, 2>(p, stream);
   }
-  if (p.group <= 8) return launch_shape<T, D, 1>(p, stream);
-  return launch_shape<T, D, 2>(p, stream);
+  if (p.chunk_len > 1) {
+    if constexpr (D == 64 || D == 128) {
+      if (p.group <= 8) return launch_shape<T, D, 1, true>(p, stream);
+      if constexpr (D == 64) return launch_shape<T, D, 2, true>(p, stream);
+    }
+    return cudaErrorInvalidValue;
+  }
+  if (p.group <= 8) return launch_shape<T, D, 1, false>(p, stream);
+  return launch_shape<T, D, 2, false>(p, stream);
 }
 
 template <typename T>
@@ -640,6 +680,13 @@ cudaError_t launch_typed(const DecodeParams &p, cudaStream_t stream) {
 }
 
 }  // namespace
+
+// Up to 16 columns at head_dim 64 and 8 at head_dim 128: with 16 columns at
+// head_dim 128 (two n-tiles, 160+ registers) the chunk kernel measured faster.
+bool mma_chunk_supports(pa_dtype dtype, int head_dim, int columns) {
+  if (dtype != PA_F16 && dtype != PA_BF16) return false;
+  return (head_dim == 64 && columns <= 16) || (head_dim == 128 && columns <= 8);
+}
 
 bool mma_supports(pa_dtype dtype, int head_dim, int group) {
   if (dtype != PA_F16 && dtype != PA_BF16) return false;

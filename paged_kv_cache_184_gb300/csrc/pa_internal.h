@@ -51,6 +51,12 @@ struct DecodeParams {
   const int32_t *items;     // work list [num_items][4] (pa_decode_work), else null
   int32_t num_items;
   float scale_log2;         // scale * log2(e): scores kept in base-2 units
+  // Chunked read on this kernel (tensor-core read, chunk_len > 1): `group`
+  // counts the CTA's columns, chunk_len * head_group (query, head) pairs, and
+  // column c is query c / head_group, head c % head_group of the kv head;
+  // q and out are [B][chunk_len][Hq][D], the partials [B][chunk_len][Hq][S][D].
+  int32_t chunk_len;        // 1 for the single-query read
+  int32_t head_group;       // query heads per kv head (Hq / Hkv)
 };
 
 // Arguments of the chunked multi-query read (pa_decode_chunk).
@@ -90,6 +96,9 @@ struct MergeParams {
 cudaError_t launch_decode_simt(const DecodeParams &p, pa_dtype dtype, cudaStream_t stream);
 // Tensor-core read: f16/bf16, head_dim in {32, 48, 64, 96, 128, 256}, groups of up to 16.
 bool mma_supports(pa_dtype dtype, int head_dim, int group);
+// The chunked read of up to 16 (query, head) columns per kv head at head_dim
+// 64, or 8 at head_dim 128, on the tensor-core decode kernel (f16/bf16).
+bool mma_chunk_supports(pa_dtype dtype, int head_dim, int columns);
 cudaError_t launch_decode_mma(const DecodeParams &p, pa_dtype dtype, cudaStream_t stream);
 // Tensor-core read over a planned work list (p.items), same shapes as above.
 cudaError_t launch_decode_items(const DecodeParams &p, pa_dtype dtype, cudaStream_t stream);

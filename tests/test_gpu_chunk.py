@@ -200,6 +200,9 @@ def test_prefill_4096_sampled_rows(lib):
     ("bf16", 32, 2, 128, 16, 16, [16, 17, 300, 2500]),       # group 16
     ("f16", 16, 4, 64, 16, 96, [30, 96, 200, 700]),          # queries at negative positions
     ("bf16", 32, 8, 64, 32, 128, [128, 129, 1024, 4096]),    # 512 rows, pages of 32
+    ("bf16", 32, 8, 64, 128, 64, [64, 300, 1000, 1500]),     # pages of 128: two copies per page
+    ("f16", 32, 8, 128, 256, 80, [80, 500, 700, 1300]),      # pages of 256, head_dim 128
+    ("bf16", 32, 8, 64, 4, 64, [64, 99, 300, 650]),          # pages of 4: cp.async for every tile
 ])
 def test_warp_specialized_chunks(lib, dtype, hq, hkv, d, bs, n_q, lens):
     pages = sum(-(-n // bs) for n in lens) + 5
@@ -232,3 +235,25 @@ def test_warp_specialized_bad_page_is_reported_and_zeroed(lib):
     assert int(err.item()) == 1
     assert torch.all(out[2] == 0)
     assert_attn_close(out[:2], _ref(base, q, [0, 1]), base.dtype)
+
+
+# ---- up to 16 (query, head) columns per kv head (8 at head_dim 128): the decode kernel, per-column limits
+
+
+@pytest.mark.parametrize("dtype,hq,hkv,d,bs,n_q,lens", [
+    ("bf16", 32, 8, 64, 16, 2, [2, 37, 300, 1000]),          # 8 columns
+    ("bf16", 32, 8, 64, 16, 3, [3, 16, 17, 2049]),           # 12 columns
+    ("f16", 32, 8, 128, 16, 2, [2, 5, 640, 1500]),           # 8 columns, head_dim 128
+    ("bf16", 32, 4, 64, 8, 2, [9, 64, 65, 700]),             # group 8: 16 columns, pages of 8
+    ("bf16", 16, 8, 128, 32, 4, [1, 2, 100, 900]),           # group 2; queries at negative positions
+])
+def test_small_chunks_on_the_decode_kernel(lib, dtype, hq, hkv, d, bs, n_q, lens):
+    pages = sum(-(-n // bs) for n in lens) + 5
+    base = workloads.make_batch("small", 49, dtype, lens, hq, hkv, d, bs, pages)
+    assert n_q * (hq // hkv) <= 16
+    q = _chunk_batch(base, n_q)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = _run(lib, base, q, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_attn_close(out, _ref(base, q), base.dtype)

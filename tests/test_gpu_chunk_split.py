@@ -76,6 +76,10 @@ def _check_partials(po, pl, ref_po, ref_pl, dtype, what=""):
     ("bf16", 16, 4, 64, 16, 48, [20, 48, 130, 640], 1),      # queries at negative positions
     ("bf16", 32, 8, 64, 16, 80, [80, 90, 700, 1300], 3),     # 320 rows: warp-specialized
     ("f16", 32, 8, 128, 16, 64, [64, 200, 900, 1100], 8),    # 256 rows, head_dim 128
+    ("bf16", 32, 8, 64, 128, 64, [64, 300, 1000, 1500], 1),  # pages of 128, one per split
+    ("bf16", 32, 8, 64, 16, 64, [64, 300, 1000, 1500], 5),   # splits of 80 tokens: tiles off 64
+    ("f16", 32, 8, 128, 16, 2, [3, 50, 700, 1600], 2),       # 8 columns on the decode kernel
+    ("bf16", 32, 4, 64, 16, 2, [1, 40, 333, 1200], 3),       # group 8, a query at position -1
 ])
 def test_partials_and_merge(lib, dtype, hq, hkv, d, bs, n_q, lens, pps):
     pages = sum(-(-n // bs) for n in lens) + 5
@@ -149,3 +153,15 @@ def test_longctx_32k_sampled(lib, n_q):
                 ref, _ = oracle.attend(host_f32(q[b, i, h]), k[:seen, h // 4], v[:seen, h // 4],
                                        g.scale)
                 assert_attn_close(out[b, i, h], ref, g.dtype, f"b{b} i{i} h{h}")
+
+
+def test_small_chunk_many_splits_per_cta(lib):
+    # few (sequence, kv head) pairs and many splits: the decode kernel covers several
+    # consecutive splits per CTA, here with 2 queries x 4 heads per kv head
+    base = workloads.make_batch("chunk_multi", 55, "bf16", [8192, 5000], 16, 4, 128, 16, 900)
+    q = _q(base, 2)
+    g = base.to(DEV)
+    po, pl, out = _split(lib, g, q.to(DEV), 2)
+    ref_po, ref_pl = _oracle_partials(base, q, 2, po.shape[3])
+    _check_partials(po, pl, ref_po, ref_pl, base.dtype, "many splits")
+    assert_attn_close(out, _oracle_chunk(base, q), base.dtype, "merged")
