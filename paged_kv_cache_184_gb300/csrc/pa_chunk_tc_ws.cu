@@ -413,30 +413,53 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const uint32_t t_s = t_s0 + (j & 1) * kKeyTile;
+      const int tok0 = t_lo + j * kKeyTile;
       float s[kKeyTile];
-      if (warp_live) {
+      // S row of this thread, -inf past its last key
+      auto load_s = [&]() {
         tmem_ld64(t_s, s);
-        const int tok0 = t_lo + j * kKeyTile;
         if (tok0 + kKeyTile - 1 > pos) {  // the tile crosses this row's last key
 #pragma unroll
           for (int c = 0; c < kKeyTile; ++c)
             if (tok0 + c > pos) s[c] = -CUDART_INF_F;
         }
-      }
+      };
+      if (warp_live) load_s();
       const bool turns = D > 64 && j < n_pair;
       if (turns && (k == 1 || j > 0) &&
           !wait_phase(smem_u32(&bar_turn[k]), (k == 0 ? j - 1 : j) & 1))
         fail = true;
       float alpha = 1.f;
       if (warp_live && !fail) {
-        const float mx = row_max64(s);
-        if (mx != -CUDART_INF_F &&
-            (m_ref == -CUDART_INF_F || (mx - m_ref) * sl2 > kRescaleLog2)) {
-          alpha = m_ref == -CUDART_INF_F ? 0.f : ex2_approx((m_ref - mx) * sl2);
-          m_ref = mx;
+        float sum = 0.f;
+        bool full = true;  // take the lazy rule (and the row max)
+        if constexpr (D == 64) {
+          // Common case first: exponents against the current reference.  When
+          // their sum is at most 2^8 no probability exceeds 2^8, so the rule
+          // would not move the reference and the row max is not needed.
+          // Otherwise (or on a first tile) the warp reloads S and takes the
+          // rule.  (At head_dim 128, with its registers nearly all in use, the
+          // extra path measured slower.)
+          full = j == 0 || m_ref == -CUDART_INF_F;
+          if (!__any_sync(0xffffffffu, full)) {
+            sum = row_exp64(s, sl2, m_ref * sl2);
+            full = !(sum <= 256.f);
+          }
+          full = __any_sync(0xffffffffu, full);
+          if (full && j > 0) load_s();  // the fast attempt overwrote s (warp-collective)
         }
-        const float mu = m_ref == -CUDART_INF_F ? 0.f : m_ref * sl2;
-        const float sum = row_exp64(s, sl2, mu);  // masked: 2^-inf = 0
+        if (full) {
+          // the lazy rule: the reference max moves only when a score passes it
+          // by more than 2^8
+          const float mx = row_max64(s);
+          if (mx != -CUDART_INF_F &&
+              (m_ref == -CUDART_INF_F || (mx - m_ref) * sl2 > kRescaleLog2)) {
+            alpha = m_ref == -CUDART_INF_F ? 0.f : ex2_approx((m_ref - mx) * sl2);
+            m_ref = mx;
+          }
+          const float mu = m_ref == -CUDART_INF_F ? 0.f : m_ref * sl2;
+          sum = row_exp64(s, sl2, mu);  // masked: 2^-inf = 0
+        }
         l = fmaf(l, alpha, sum);
       }
       if (turns) {
