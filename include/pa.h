@@ -242,6 +242,12 @@ pa_status pa_decode_work(float *partial_out, float *partial_lse, const int32_t *
  * rows); chunks of one query, or of up to 16 (query, head) columns per kv
  * head at head_dim 64 (8 at head_dim 128), on the single-query read's kernel
  * with a causal limit per column; the rest on the mma.sync chunk kernel.
+ *
+ * The tcgen05 reads wait on mbarriers with a bound (about a second per wait);
+ * a wait that runs out records PA_DEV_TIMEOUT in *dev_err, the affected
+ * outputs are zeroed and the context stays usable.  Test hook: with the
+ * environment variable PA_TEST_WITHHOLD_TILES=1 the warp-specialized read
+ * (256+ rows per kv head) loads no key tile, so that path can be exercised.
  */
 pa_status pa_decode_chunk(void *out, const void *q, const void *k_pool,
                           const void *v_pool, const int32_t *block_table,

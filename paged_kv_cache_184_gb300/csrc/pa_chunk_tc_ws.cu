@@ -36,6 +36,7 @@
 #include <cuda.h>  // CUtensorMap (the encoder is fetched through the runtime)
 #include <math_constants.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "pa_common.cuh"
@@ -99,7 +100,8 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     chunk_tc_ws_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tmap_k,
-                       const __grid_constant__ CUtensorMap tmap_v, const int use_tma) {
+                       const __grid_constant__ CUtensorMap tmap_v, const int use_tma,
+                       const int withhold) {
   using S = WsShape<D>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ uint64_t bar_full[kStages], bar_empty[kStages];
@@ -257,7 +259,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     int pa, pb;
     fetch_pages(loader, pa, pb);
-    for (int j = loader; j < ntiles; j += kLoaders) {
+    // test hook: no tile is ever announced, so the other roles' waits run out
+    for (int j = loader; j < ntiles && !withhold; j += kLoaders) {
       const int st = j % kStages;
       if (j >= kStages && !wait_phase(smem_u32(&bar_empty[st]), ((j / kStages) - 1) & 1)) {
         fail = true;
@@ -615,9 +618,15 @@ cudaError_t launch_d(const ChunkParams &p, pa_dtype dtype, cudaStream_t stream) 
   CUtensorMap mk{}, mv{};
   const int use_tma = p.block_size_log2 >= 3 && make_pool_map(&mk, p.k_pool, dtype, p) &&
                       make_pool_map(&mv, p.v_pool, dtype, p);
+  // Test hook for the time-out path: PA_TEST_WITHHOLD_TILES=1 makes the load
+  // warps announce no tile; every wait then runs out (at most 2^26 polls of
+  // 20 ns each, per CTA) and the call reports PA_DEV_TIMEOUT with zeroed
+  // outputs.  Nothing is in flight when the waits give up.
+  const char *hold = std::getenv("PA_TEST_WITHHOLD_TILES");
+  const int withhold = hold != nullptr && hold[0] == '1' && hold[1] == '\0';
   const int nblk = (p.chunk_len * p.group + kCtaRows - 1) / kCtaRows;
   dim3 grid(nblk * p.num_kv_heads, p.num_seqs, p.partial_out ? p.num_splits : 1);
-  return launch_pdl(kern, grid, dim3(kThreads), smem, stream, p, mk, mv, use_tma);
+  return launch_pdl(kern, grid, dim3(kThreads), smem, stream, p, mk, mv, use_tma, withhold);
 }
 
 template <typename T>

@@ -15,9 +15,18 @@
 namespace pa {
 namespace tc {
 
-// Polls of an mbarrier before a wait gives up (and the kernel reports
-// PA_DEV_TIMEOUT instead of hanging).
+// A wait on an mbarrier gives up (and the kernel reports PA_DEV_TIMEOUT
+// instead of hanging) after about a second, or after kSpinLimit polls,
+// whichever comes first.  A poll that finds the phase incomplete may suspend
+// the thread for microseconds, so the time bound is the one that acts.
 constexpr uint32_t kSpinLimit = 1u << 26;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   uint64_t d = static_cast<uint64_t>((saddr >> 4) & 0x3FFF);
@@ -62,10 +71,11 @@ __device__ __forceinline__ void commit(uint32_t mbar) {
                : "memory");
 }
 
-// Wait for the given phase of an mbarrier; false after kSpinLimit polls.
-// Each poll may suspend the thread for at most 20 ns (the explicit hint
-// measured a few per cent faster than the default limit).
+// Wait for the given phase of an mbarrier; false once the bounds above are
+// reached.  Each poll passes a 20 ns suspend hint (measured a few per cent
+// faster than the default limit).
 __device__ __forceinline__ bool wait_phase(uint32_t mbar, uint32_t phase) {
+  uint64_t t0 = 0;
   for (uint32_t it = 0; it < kSpinLimit; ++it) {
     uint32_t done;
     asm volatile(
@@ -75,6 +85,11 @@ __device__ __forceinline__ bool wait_phase(uint32_t mbar, uint32_t phase) {
         : "r"(mbar), "r"(phase)
         : "memory");
     if (done) return true;
+    if (it == 0) {
+      t0 = global_ns();
+    } else if ((it & 15) == 0 && global_ns() - t0 > kWaitLimitNs) {
+      return false;
+    }
   }
   return false;
 }
