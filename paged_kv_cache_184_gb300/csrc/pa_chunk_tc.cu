@@ -3,10 +3,11 @@
 //
 // Same contract as the mma.sync chunk read (nanoserve "Day 23: the real
 // triton.jit paged-attention kernel": query i of a chunk sits at position
-// past + i and sees tokens 0 .. past + i), for chunks long enough to fill
-// 128-row tiles: a prompt's prefill is the chunk that starts at past = 0.
-// One CTA owns 128 (query, head) rows of one (sequence, kv head), one row
-// per thread, and walks the causal key range in 64-token tiles:
+// past + i and sees tokens 0 .. past + i), for chunks of 64 to 255 (query,
+// head) rows per kv head at head_dim 64 and 128 to 255 at head_dim 128;
+// longer ones (a prompt's prefill among them) go to the warp-specialized
+// read.  One CTA owns 128 rows of one (sequence, kv head), one row per
+// thread, and walks the causal key range in 64-token tiles:
 //
 //   S [128 x 64] = Q [128 x D] . K_tile^T      tcgen05.mma -> tensor memory
 //   softmax      : thread r loads row r of S (tcgen05.ld), masks, takes the

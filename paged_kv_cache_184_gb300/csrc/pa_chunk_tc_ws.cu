@@ -7,32 +7,38 @@
 // P rounded to the cache dtype), but the phases of a key tile run on
 // different warps at the same time instead of one after the other:
 //
-//   warps 0, 3   load: 64-token K/V tiles (alternately) through the block
+//   warps 0, 3   load, alternately, 64-token K/V tiles through the block
 //                table ("Three Attention Kernels", section "3. Paged KV-cache
-//                attention") into a 4-stage ring, 16-byte cp.async with
-//                zero-fill past the end; a tile is announced on its `full`
-//                mbarrier once the warp's own copies have landed
+//                attention") into a 4-stage ring: a tile whose tokens all
+//                exist by 2D tensor-map copies (cp.async.bulk.tensor, one per
+//                page and head_dim half, counted in bytes on the stage's
+//                `full` mbarrier); the last tile of a range (or pages of
+//                fewer than 8 tokens) by 16-byte cp.async with zero-fill,
+//                announced once the warp's own copies have landed
 //   warps 1, 2   MMA: lane 0 of warp 1 + k issues S_k = Q_k . K^T and
 //                O_k += P_k . V for Q tile k (tcgen05.mma, fp32 accumulators
-//                in tensor memory) and commits each to an mbarrier
+//                in tensor memory) and commits each to an mbarrier; QK(j + 2)
+//                goes right after P.V(j), into the S buffer P.V(j) has read
 //   warps 4-7    softmax of Q tile 0, warps 8-11 of Q tile 1: thread r of a
 //                group owns row r (tensor-memory lane r), reads its S row,
 //                writes its P row back over S as 16-bit pairs, and moves
 //                the reference max (rescaling its O row) only when a score
 //                passes it by more than 2^8
 //
-// While the softmax warps of one Q tile work on key tile j, the tensor core
-// runs the other tile's products and the load warp fetches tiles j+1, j+2.
-// Two Q tiles share every K/V tile, so each copy feeds twice the math.
+// While the softmax warps of one Q tile work on key tile j, S(j + 1) is
+// already in tensor memory, the tensor core runs the other products, and
+// the load warps fetch the next tiles.  Two Q tiles share every K/V tile, so
+// each copy feeds twice the math.
 //
-// Tensor memory: S_0 | S_1 (64 columns each) | O_0 | O_1 (head_dim each).
-// mbarriers: full/empty per ring stage, and per Q tile and S buffer s (S
-// ready), p (P written, one arrival per softmax warp), o (P.V done: the
-// buffer and O free again).  One barrier per buffer means no waiter can see a
-// barrier complete twice before it looks (parity waits would misread that).
-// Every wait is
-// bounded; on time-out the kernel records PA_DEV_TIMEOUT, every role leaves
-// its loop, the outputs are zeroed and the tensor memory is freed.
+// Tensor memory: S_0[0..1] | S_1[0..1] (64 columns each) | O_0 | O_1
+// (head_dim each).  mbarriers: full/empty per ring stage, and per Q tile and
+// S buffer s (S ready), p (P written, one arrival per softmax warp), o (P.V
+// done: the buffer and O free again); at head_dim 128 also one per softmax
+// group for taking turns at the exponentials.  One barrier per buffer means
+// no waiter can see a barrier complete twice before it looks (parity waits
+// would misread that).  Every wait is bounded (about a second); on time-out
+// the kernel records PA_DEV_TIMEOUT, every role leaves its loop, the outputs
+// are zeroed and the tensor memory is freed.
 #include <cuda.h>  // CUtensorMap (the encoder is fetched through the runtime)
 #include <math_constants.h>
 
