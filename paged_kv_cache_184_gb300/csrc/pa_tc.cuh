@@ -94,6 +94,27 @@ __device__ __forceinline__ bool wait_phase(uint32_t mbar, uint32_t phase) {
   return false;
 }
 
+// The wait for tcgen05.ld / tcgen05.st, with 32 registers tied to it: the
+// registers a load writes are read only after the wait, and the registers a
+// store reads keep their values (are not reused) until the wait.
+#define PA_TIE32(q)                                                                        \
+  "+r"(q[0]), "+r"(q[1]), "+r"(q[2]), "+r"(q[3]), "+r"(q[4]), "+r"(q[5]), "+r"(q[6]),      \
+      "+r"(q[7]), "+r"(q[8]), "+r"(q[9]), "+r"(q[10]), "+r"(q[11]), "+r"(q[12]),           \
+      "+r"(q[13]), "+r"(q[14]), "+r"(q[15]), "+r"(q[16]), "+r"(q[17]), "+r"(q[18]),        \
+      "+r"(q[19]), "+r"(q[20]), "+r"(q[21]), "+r"(q[22]), "+r"(q[23]), "+r"(q[24]),        \
+      "+r"(q[25]), "+r"(q[26]), "+r"(q[27]), "+r"(q[28]), "+r"(q[29]), "+r"(q[30]),        \
+      "+r"(q[31])
+
+__device__ __forceinline__ void wait_ld_tied(uint32_t *q) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : PA_TIE32(q)::"memory");
+}
+
+__device__ __forceinline__ void wait_st_tied(uint32_t *q) {
+  asm volatile("tcgen05.wait::st.sync.aligned;" : PA_TIE32(q)::"memory");
+}
+
+__device__ __forceinline__ void tie32(uint32_t *q) { asm volatile("" : PA_TIE32(q)); }
+
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
   uint32_t r[32];
   asm volatile(
@@ -105,7 +126,7 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
         "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  wait_ld_tied(r);
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
 }
@@ -126,7 +147,8 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float *v) {
           "=r"(q[26]), "=r"(q[27]), "=r"(q[28]), "=r"(q[29]), "=r"(q[30]), "=r"(q[31])
         : "r"(taddr + 32 * h));
   }
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  wait_ld_tied(r);
+  tie32(r + 32);  // after the wait, too
 #pragma unroll
   for (int j = 0; j < 64; ++j) v[j] = __uint_as_float(r[j]);
 }
@@ -140,7 +162,10 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float *v) {
       "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]),
       "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]),
       "f"(v[29]), "f"(v[30]), "f"(v[31]));
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+  uint32_t q[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) q[j] = __float_as_uint(v[j]);
+  wait_st_tied(q);
 }
 
 __device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t *v) {
@@ -152,7 +177,10 @@ __device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t *v) {
       "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
       "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
       "r"(v[29]), "r"(v[30]), "r"(v[31]));
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+  uint32_t q[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) q[j] = v[j];
+  wait_st_tied(q);
 }
 
 template <typename T> struct Pack2;
