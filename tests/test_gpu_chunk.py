@@ -246,6 +246,7 @@ def test_warp_specialized_bad_page_is_reported_and_zeroed(lib):
     ("f16", 32, 8, 128, 16, 2, [2, 5, 640, 1500]),           # 8 columns, head_dim 128
     ("bf16", 32, 4, 64, 8, 2, [9, 64, 65, 700]),             # group 8: 16 columns, pages of 8
     ("bf16", 16, 8, 128, 32, 4, [1, 2, 100, 900]),           # group 2; queries at negative positions
+    ("bf16", 8, 8, 64, 16, 16, [16, 17, 500, 1234]),         # group 1: 16 queries, one head each
 ])
 def test_small_chunks_on_the_decode_kernel(lib, dtype, hq, hkv, d, bs, n_q, lens):
     pages = sum(-(-n // bs) for n in lens) + 5

@@ -80,6 +80,7 @@ def _check_partials(po, pl, ref_po, ref_pl, dtype, what=""):
     ("bf16", 32, 8, 64, 16, 64, [64, 300, 1000, 1500], 5),   # splits of 80 tokens: tiles off 64
     ("f16", 32, 8, 128, 16, 2, [3, 50, 700, 1600], 2),       # 8 columns on the decode kernel
     ("bf16", 32, 4, 64, 16, 2, [1, 40, 333, 1200], 3),       # group 8, a query at position -1
+    ("bf16", 8, 8, 64, 16, 16, [16, 300, 900, 1111], 4),     # group 1: 16 queries, one head each
 ])
 def test_partials_and_merge(lib, dtype, hq, hkv, d, bs, n_q, lens, pps):
     pages = sum(-(-n // bs) for n in lens) + 5
