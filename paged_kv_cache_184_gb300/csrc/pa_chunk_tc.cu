@@ -104,7 +104,10 @@ __global__ void __launch_bounds__(kThreads, TcShape<D>::kMinBlocks)
   int len = __ldg(p.seq_lens + b);
   const long long cap = static_cast<long long>(p.max_blocks) << bs_log2;
   const bool bad_len = (len < 0) || (static_cast<long long>(len) > cap);
-  if (bad_len) len = 0;
+  if (bad_len) {
+    if (threadIdx.x == 0) report_error(p.dev_err, PA_DEV_BAD_SEQ_LEN);
+    len = 0;
+  }
   const int past = len - nq;
   // tokens [t_lo, t_hi) of this CTA: the whole sequence, or one split of it
   int t_lo = 0, t_hi = len;

@@ -277,3 +277,18 @@ def test_warp_specialized_wait_time_out_is_reported(lib, monkeypatch):
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     assert_attn_close(out, _ref(base, q), base.dtype)
+
+
+@pytest.mark.parametrize("n_q", [40, 80])        # 160 rows: single-tile kernel; 320: warp-specialized
+def test_tensor_core_bad_seq_len_is_reported_and_zeroed(lib, n_q):
+    base = workloads.make_batch("tclen", 51, "bf16", [100, 300], 32, 8, 64, 16, 40)
+    q = _chunk_batch(base, n_q)
+    good = base.seq_lens.clone()
+    base.seq_lens[1] = base.max_blocks * base.block_size + 1   # past the table's capacity
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = _run(lib, base, q, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == lib.PA_DEV_BAD_SEQ_LEN
+    assert torch.all(out[1] == 0)
+    base.seq_lens = good
+    assert_attn_close(out[:1], _ref(base, q, [0]), base.dtype)
