@@ -241,3 +241,25 @@ def test_chunk_splitkv_validation(lib, kw, want):
         a["hq"], a["hkv"], a["d"], a["bs"], a["np_"], a["scale"], a["pps"], a["ms"], a["dt"],
         None, None)
     assert st == want
+
+
+def test_binding_merge_and_chunk_split_shape_checks(lib):
+    # shape checks of the binding raise before any pointer is taken or any call is made
+    import torch
+    po = torch.zeros(2, 3, 4, 5, 64)              # [B, n_q, Hq, S, d]
+    pl = torch.zeros(2, 3, 4, 5)
+    with pytest.raises(ValueError):                # out must be [B, n_q, Hq, d]
+        lib.pa_merge(torch.zeros(2, 3, 4, 32, dtype=torch.bfloat16), po, pl)
+    with pytest.raises(ValueError):                # lse must match the leading axes
+        lib.pa_merge(torch.zeros(2, 3, 4, 64, dtype=torch.bfloat16), po, torch.zeros(2, 3, 5, 5))
+    with pytest.raises(ValueError):                # partials need at least [B, Hq, S, d]
+        lib.pa_merge(torch.zeros(4, 64), torch.zeros(4, 5, 64), torch.zeros(4, 5))
+    q = torch.zeros(2, 3, 4, 64, dtype=torch.bfloat16)
+    kp = torch.zeros(8, 16, 1, 64, dtype=torch.bfloat16)
+    bt = torch.zeros(2, 4, dtype=torch.int32)
+    sl = torch.ones(2, dtype=torch.int32)
+    with pytest.raises(ValueError):                # partials [B, n_q, Hq, S, d] with S = lse's
+        lib.pa_decode_chunk_splitkv(torch.zeros(2, 3, 4, 6, 64), pl, q, kp, kp, bt, sl, 0.125, 1)
+    with pytest.raises(ValueError):                # head_dim of q and the pools must agree
+        lib.pa_decode_chunk_splitkv(po, pl, torch.zeros(2, 3, 4, 32, dtype=torch.bfloat16), kp,
+                                    kp, bt, sl, 0.125, 1)
