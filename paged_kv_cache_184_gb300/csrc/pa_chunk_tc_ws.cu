@@ -580,7 +580,7 @@ using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t,
                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-// the driver's tensor-map encoder, looked up once (null if unavailable)
+// the CUDA driver's tensor-map encoder, looked up once (null if unavailable)
 EncodeTiled encoder() {
   static EncodeTiled fn = nullptr;
   static std::once_flag once;
