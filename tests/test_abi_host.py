@@ -160,6 +160,16 @@ def test_binding_rejects_host_tensors(lib):
         lib.pa_decode(torch.empty_like(q), q, kp, kp, bt, sl, 0.125)
 
 
+def test_missing_library_raises_with_no_fallback(lib, monkeypatch, tmp_path):
+    # the binding has no other implementation: without libpa.so every entry point fails
+    monkeypatch.setattr(pa, "_lib", None)
+    monkeypatch.setattr(pa, "LIB_PATH", str(tmp_path / "libpa.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        pa.load(build=False)
+    with pytest.raises(RuntimeError, match="not built"):
+        pa.pa_num_splits(10, 2)
+
+
 def test_binding_raises_on_bad_status(lib):
     assert isinstance(pa.PaError("pa_decode", 2), RuntimeError)
     assert "PA_ERR_UNSUPPORTED" in str(pa.PaError("pa_decode", 2))
