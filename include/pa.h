@@ -242,6 +242,8 @@ pa_status pa_decode_work(float *partial_out, float *partial_lse, const int32_t *
  * rows); chunks of one query, or of up to 16 (query, head) columns per kv
  * head at head_dim 64 (8 at head_dim 128), on the single-query read's kernel
  * with a causal limit per column; the rest on the mma.sync chunk kernel.
+ * chunk_len * (num_q_heads / num_kv_heads) above 2^30 (query, head) rows
+ * per kv head returns PA_ERR_UNSUPPORTED.
  *
  * The tcgen05 reads wait on mbarriers with a bound (about a second per wait);
  * a wait that runs out records PA_DEV_TIMEOUT in *dev_err, the affected

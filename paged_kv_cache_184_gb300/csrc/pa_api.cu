@@ -18,6 +18,8 @@ constexpr int32_t kMaxGroupSimt = 8;   // CUDA-core read
 constexpr int32_t kMaxGroupMma = 16;   // tensor-core read
 constexpr int32_t kMaxBlockSize = 1024;
 constexpr int32_t kMaxSeqs = 65535;  // grid.y
+// (query, head) rows per kv head of a chunk: an int in the kernels, with room for rounding up
+constexpr int64_t kMaxChunkRows = int64_t{1} << 30;
 
 int elem_size(pa_dtype dt) {
   switch (dt) {
@@ -261,6 +263,7 @@ pa_status pa_decode_chunk(void *out, const void *q, const void *k_pool, const vo
   if (st != PA_OK) return st;
   if (!pa::chunk_supports(dtype, head_dim)) return PA_ERR_UNSUPPORTED;
   const int64_t rows = static_cast<int64_t>(chunk_len) * (num_q_heads / num_kv_heads);
+  if (rows > kMaxChunkRows) return PA_ERR_UNSUPPORTED;
   const int64_t ctas = (rows + pa::chunk_rows_per_cta() - 1) / pa::chunk_rows_per_cta();
   if (ctas * num_kv_heads > INT32_MAX) return PA_ERR_UNSUPPORTED;
   if (num_seqs == 0) return PA_OK;
@@ -271,7 +274,7 @@ pa_status pa_decode_chunk(void *out, const void *q, const void *k_pool, const vo
   const int group = num_q_heads / num_kv_heads;
   // one query per sequence is the single-query read; up to 16 (query, head)
   // columns per kv head run on its tensor-core kernel with per-column limits
-  if (chunk_len == 1 || pa::mma_chunk_supports(dtype, head_dim, chunk_len * group)) {
+  if (chunk_len == 1 || pa::mma_chunk_supports(dtype, head_dim, static_cast<int>(rows))) {
     pa::DecodeParams dp = make_params(q, k_pool, v_pool, block_table, max_blocks_per_seq,
                                       seq_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
                                       block_size, num_pages, scale, dev_err);
@@ -320,6 +323,7 @@ pa_status pa_decode_chunk_splitkv(float *partial_out, float *partial_lse, const 
   if (max_splits < need) return PA_ERR_INVALID_ARG;
   if (max_splits > 65535) return PA_ERR_UNSUPPORTED;  // the split is the grid's z index
   const int64_t rows = static_cast<int64_t>(chunk_len) * (num_q_heads / num_kv_heads);
+  if (rows > kMaxChunkRows) return PA_ERR_UNSUPPORTED;
   const int64_t ctas = (rows + pa::chunk_rows_per_cta() - 1) / pa::chunk_rows_per_cta();
   if (ctas * num_kv_heads > INT32_MAX) return PA_ERR_UNSUPPORTED;
   if (num_seqs == 0) return PA_OK;
@@ -329,7 +333,7 @@ pa_status pa_decode_chunk_splitkv(float *partial_out, float *partial_lse, const 
     return PA_ERR_INVALID_ARG;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int group = num_q_heads / num_kv_heads;
-  if (chunk_len == 1 || pa::mma_chunk_supports(dtype, head_dim, chunk_len * group)) {
+  if (chunk_len == 1 || pa::mma_chunk_supports(dtype, head_dim, static_cast<int>(rows))) {
     pa::DecodeParams dp = make_params(q, k_pool, v_pool, block_table, max_blocks_per_seq,
                                       seq_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
                                       block_size, num_pages, scale, dev_err);

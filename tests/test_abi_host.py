@@ -201,6 +201,9 @@ def test_noalloc_validation_before_any_device_call(lib, kw, want):
     (dict(q=MISALIGNED), pa.PA_ERR_INVALID_ARG),
     (dict(b=0), pa.PA_OK),
     (dict(b=0, hq=16, hkv=1, nq=4096), pa.PA_OK),
+    # (query, head) rows per kv head past 2^30 are refused before any 32-bit product
+    (dict(nq=(1 << 28) + 1), pa.PA_ERR_UNSUPPORTED),
+    (dict(nq=2**31 - 1, hq=16, hkv=1), pa.PA_ERR_UNSUPPORTED),
 ])
 def test_chunk_validation(lib, kw, want):
     a = dict(out=FAKE, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, mb=4, sl=FAKE, b=2, nq=8, hq=8, hkv=2,
@@ -241,6 +244,7 @@ def test_work_validation(lib, kw, want):
     (dict(po=MISALIGNED), pa.PA_ERR_INVALID_ARG),
     (dict(pl=None), pa.PA_ERR_INVALID_ARG),
     (dict(b=0), pa.PA_OK),
+    (dict(nq=2**31 - 1, hq=16, hkv=1), pa.PA_ERR_UNSUPPORTED),
 ])
 def test_chunk_splitkv_validation(lib, kw, want):
     a = dict(po=FAKE, pl=FAKE, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, mb=4, sl=FAKE, b=2, nq=8, hq=8,
