@@ -1,0 +1,58 @@
+"""bench.py's host-side pieces that need no GPU: the roofline denominators
+and the ncu traffic figure it reports beside the achieved bandwidth."""
+
+import json
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def test_peaks_fall_back_without_a_measured_file(monkeypatch, tmp_path):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.measured_peaks() == (bench.FALLBACK_HBM_GBS, "fallback")
+    assert bench.measured_bf16_tflops() == (1900.0, "fallback")
+
+
+def test_peaks_come_from_the_measured_file(monkeypatch, tmp_path):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps(
+        {"hbm_gbs": 7012.5, "bf16_tflops": 1911.0, "bf16_tflops_sustained": 1702.0,
+         "clocks": {"sm_mhz": 2070}}))
+    assert bench.measured_peaks() == (7012.5, "measured")
+    # the burst figure: the prefill kernel is timed alone, not inside a long step
+    assert bench.measured_bf16_tflops() == (1911.0, "measured")
+
+
+def test_unreadable_peaks_file_falls_back(monkeypatch, tmp_path):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (tmp_path / "MEASURED_PEAKS.json").write_text("{not json")
+    assert bench.measured_peaks()[1] == "fallback"
+    assert bench.measured_bf16_tflops()[1] == "fallback"
+
+
+def test_committed_profile_describes_the_current_read_kernel():
+    # the traffic figure is reported only while the profile's source hash matches the
+    # kernel source it was captured from
+    traffic = bench.profiled_traffic()
+    assert traffic is not None, "profile's source_sha no longer matches the read kernel"
+    algorithmic = bench.read_bytes([4096] * 64, 32, 8, 64, 2, 16)
+    assert algorithmic == 537_460_992
+    assert 1.0 <= traffic / algorithmic < 1.05
+
+
+def test_stale_profile_reports_no_traffic(monkeypatch):
+    monkeypatch.setattr(bench, "source_sha", lambda: "0" * 16)
+    assert bench.profiled_traffic() is None
+
+
+@pytest.mark.parametrize("lens,want", [
+    ([1], 1 * 8 * 64 * 2 * 2 + 2 * 32 * 64 * 2 + 4 * 1 + 4),
+    ([16, 17], 33 * 8 * 64 * 2 * 2 + 2 * 2 * 32 * 64 * 2 + 4 * 3 + 4 * 2),
+])
+def test_read_bytes_counts_kv_q_out_table_and_lengths(lens, want):
+    assert bench.read_bytes(lens, 32, 8, 64, 2, 16) == want
