@@ -7,7 +7,10 @@ splits' exp(lse) against the whole range's, and planted mistakes in the
 causal clip of a split.
 """
 
+import json
 import math
+import os
+from fractions import Fraction
 
 import numpy as np
 import pytest
@@ -16,6 +19,26 @@ import oracle
 import oracle.paged_attention as opa
 
 from test_oracle_chunk_pins import _random
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_worked_chunk_split.json")
+
+
+def _exact(x):
+    """Fixture values: numbers, or strings 'a/b', 'ln x' and '-inf' for exact values."""
+    if isinstance(x, list):
+        return [_exact(e) for e in x]
+    if isinstance(x, str):
+        if x == "-inf":
+            return -math.inf
+        if x.startswith("ln "):
+            return math.log(Fraction(x[3:]))
+        return float(Fraction(x))
+    return float(x)
+
+
+def _golden_cases():
+    with open(GOLDEN) as f:
+        return json.load(f)["cases"]
 
 
 def _brute_partials(q, k_pool, v_pool, block_table, seq_lens, scale, page_size,
@@ -50,6 +73,22 @@ def _brute_partials(q, k_pool, v_pool, block_table, seq_lens, scale, page_size,
 def _case(seed=5):
     x = _random(seed, [3, 10, 17], n_q=4, nh=4, nkv=2, d=5, ps=2)
     return x
+
+
+@pytest.mark.parametrize("case", _golden_cases(), ids=lambda c: c["name"])
+def test_golden_chunk_split(case):
+    arr = lambda key: np.array(_exact(case[key]))
+    part, lse = oracle.chunk_splitkv_partials(
+        arr("q"), arr("k_pool"), arr("v_pool"), np.array(case["block_table"]),
+        np.array(case["seq_lens"]), case["scale"], case["page_size"], case["pages_per_split"],
+        case["num_splits"])
+    want_lse = arr("expected_partial_lse")
+    np.testing.assert_array_equal(np.isneginf(lse), np.isneginf(want_lse))
+    fin = np.isfinite(want_lse)
+    np.testing.assert_allclose(lse[fin], want_lse[fin], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(part, arr("expected_partial_out"), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(oracle.merge_partials(part, lse), arr("expected_out"), rtol=0,
+                               atol=1e-12)
 
 
 def test_partials_match_explicit_loops():
@@ -134,6 +173,8 @@ MUTANTS = {
 
 def _split_pins_pass():
     try:
+        for case in _golden_cases():
+            test_golden_chunk_split(case)
         test_partials_match_explicit_loops()
         for pps in (1, 2, 3, 7, 64):
             test_merged_splits_are_the_chunked_read(pps)
