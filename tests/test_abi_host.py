@@ -35,6 +35,36 @@ def test_library_builds_and_exports_every_declared_symbol(lib):
         assert hasattr(raw, n), n
 
 
+def declared_parameters():
+    """{function: [parameter declarations]} from include/pa.h."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for name, params in re.findall(r"\b(pa_[a-z_0-9]+)\s*\(([^)]*)\)\s*;", text):
+        params = " ".join(params.split())
+        out[name] = [] if params in ("", "void") else [x.strip() for x in params.split(",")]
+    return out
+
+
+def _ctype_of(decl):
+    if "*" in decl or decl.startswith("pa_stream_t"):
+        return ctypes.c_void_p
+    for prefix, ct in (("int32_t", ctypes.c_int32), ("float", ctypes.c_float),
+                       ("pa_dtype", ctypes.c_int), ("pa_status", ctypes.c_int)):
+        if decl.startswith(prefix):
+            return ct
+    raise AssertionError(f"unmapped parameter type: {decl}")
+
+
+def test_binding_signatures_match_the_header():
+    # the ctypes argument lists have the header's arity and, position by position, its types
+    decl = declared_parameters()
+    assert set(decl) == set(pa._SIGNATURES)
+    for name, (_, args) in pa._SIGNATURES.items():
+        assert len(args) == len(decl[name]), name
+        for i, (got, d) in enumerate(zip(args, decl[name])):
+            assert got == _ctype_of(d), f"{name} argument {i}: {d}"
+
+
 def test_status_strings_and_version(lib):
     assert lib.pa_status_string(0) == "PA_OK"
     assert lib.pa_status_string(1) == "PA_ERR_INVALID_ARG"
