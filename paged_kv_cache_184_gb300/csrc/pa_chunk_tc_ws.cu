@@ -628,9 +628,9 @@ cudaError_t launch_d(const ChunkParams &p, pa_dtype dtype, cudaStream_t stream) 
   const int use_tma = p.block_size_log2 >= 3 && make_pool_map(&mk, p.k_pool, dtype, p) &&
                       make_pool_map(&mv, p.v_pool, dtype, p);
   // Test hook for the time-out path: PA_TEST_WITHHOLD_TILES=1 makes the load
-  // warps announce no tile; every wait then runs out (at most 2^26 polls of
-  // 20 ns each, per CTA) and the call reports PA_DEV_TIMEOUT with zeroed
-  // outputs.  Nothing is in flight when the waits give up.
+  // warps announce no tile; every wait then runs out (after about a second of
+  // the global timer, or 2^26 polls) and the call reports PA_DEV_TIMEOUT with
+  // zeroed outputs.  Nothing is in flight when the waits give up.
   const char *hold = std::getenv("PA_TEST_WITHHOLD_TILES");
   const int withhold = hold != nullptr && hold[0] == '1' && hold[1] == '\0';
   const int nblk = (p.chunk_len * p.group + kCtaRows - 1) / kCtaRows;
