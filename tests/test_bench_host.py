@@ -1,9 +1,11 @@
-"""bench.py's host-side pieces that need no GPU: the roofline denominators
-and the ncu traffic figure it reports beside the achieved bandwidth."""
+"""bench.py's host-side pieces that need no GPU: the roofline denominators,
+the ncu traffic figure it reports beside the achieved bandwidth, and the
+clock sampler (against a stand-in nvidia-smi that prints fixed rows)."""
 
 import json
 import os
 import sys
+import tempfile
 
 import pytest
 
@@ -56,3 +58,40 @@ def test_stale_profile_reports_no_traffic(monkeypatch):
 ])
 def test_read_bytes_counts_kv_q_out_table_and_lengths(lens, want):
     assert bench.read_bytes(lens, 32, 8, 64, 2, 16) == want
+
+
+_FAKE_SMI = """#!/bin/sh
+# stands in for nvidia-smi --query-gpu ... -lms 200: prints fixed samples, then waits
+cat <<'ROWS'
+0, 2070, 2070, 480.25, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active
+0, 2055, 2070, 501.00, 0x0000000000000004, Not Active, Not Active, Not Active, Active
+garbage line
+0, [N/A], 2070, 1.0, 0x0, Not Active, Not Active, Not Active, Not Active
+0, 1980, 2070, 510.50, 0x0000000000000008, Active, Not Active, Not Active, Not Active
+ROWS
+exec sleep 30
+"""
+
+
+def test_clock_sampler_reports_the_median_and_every_active_reason(monkeypatch, tmp_path):
+    smi = tmp_path / "nvidia-smi"
+    smi.write_text(_FAKE_SMI)
+    smi.chmod(0o755)
+    monkeypatch.setenv("PATH", f"{tmp_path}{os.pathsep}{os.environ['PATH']}")
+    monkeypatch.setattr(tempfile, "tempdir", str(tmp_path))
+    s = bench.ClockSampler(0)
+    s.start()
+    assert s.path.startswith(str(tmp_path))
+    got = s.stop()
+    assert got["samples"] == 3                      # the malformed rows are skipped
+    assert got["sm_mhz"] == 2055.0 and got["sm_min_mhz"] == 1980.0
+    assert got["sm_max_mhz"] == 2070.0
+    assert got["reasons"] == ["hw_slowdown", "sw_power_cap"]
+    assert not list(tmp_path.glob("clocks_*.csv"))  # the sample file is removed
+
+
+def test_clock_sampler_without_nvidia_smi(monkeypatch, tmp_path):
+    monkeypatch.setenv("PATH", str(tmp_path))       # an empty directory: no nvidia-smi
+    s = bench.ClockSampler(0)
+    s.start()
+    assert s.stop()["reasons"] == ["nvidia-smi unavailable"]
