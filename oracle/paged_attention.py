@@ -30,7 +30,7 @@ What it follows:
   position i of a chunk its own program and a causal offset ``past``: query
   i sits at position past + i and sees tokens 0 .. past + i.
 
-Readings where the pages are silent (each one is listed in the design notes):
+Readings where the pages are silent:
 
 * Pool layout [num_pages][page_size][num_kv_heads][head_dim] (page, then
   slot, then head).
@@ -46,7 +46,10 @@ Readings where the pages are silent (each one is listed in the design notes):
   split; query i's share of it stops at its causal limit past + i, so a
   split that starts after that limit is empty for that query.
 
-Every pin of this oracle lives in tests/test_oracle_pins.py.
+Its pins live in tests/test_oracle_pins.py (single-query read, splits, merge,
+append), tests/test_oracle_chunk_pins.py (chunked read) and
+tests/test_oracle_chunk_split_pins.py (split of a chunked read), with the
+hand-worked cases under tests/golden/.
 """
 
 from __future__ import annotations
