@@ -38,6 +38,10 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+# The CPU baseline is the oracle on one thread: hold NumPy's BLAS to one thread
+# as well (read when NumPy loads, which happens after this point).
+os.environ["OPENBLAS_NUM_THREADS"] = "1"
+
 METRIC = "paged decode attention: achieved HBM GB/s (% of GB300 peak), µs/step at B=64"
 UNIT = "GB/s"
 L2_BYTES = 129 * 2**20
@@ -211,13 +215,15 @@ class OracleSample:
         self.vp = batch_cpu.v_pool.float().numpy()
         self.bt = batch_cpu.block_table.numpy()
         self.lens = batch_cpu.lens_list()
+        self.cpu_s = 0.0
+        self.wall_s = 0.0
 
     def run(self, budget_s: float, max_seqs: int, first: int = 0):
         """Oracle over sequences first, first+1, ... until the budget is spent.
         Returns (seconds, algorithmic bytes read, sequences done)."""
         import oracle
         b = self.b
-        t0 = time.perf_counter()
+        t0, c0 = time.perf_counter(), time.process_time()
         done, nbytes = 0, 0
         while done < max_seqs:
             i = (first + done) % len(self.lens)
@@ -228,7 +234,14 @@ class OracleSample:
             done += 1
             if time.perf_counter() - t0 > budget_s:
                 break
-        return time.perf_counter() - t0, nbytes, done
+        wall = time.perf_counter() - t0
+        self.cpu_s += time.process_time() - c0   # CPU time of every thread of the process
+        self.wall_s += wall
+        return wall, nbytes, done
+
+    def cpu_per_wall(self) -> float:
+        """Average number of busy host threads over the timed oracle runs."""
+        return round(self.cpu_s / self.wall_s, 2) if self.wall_s > 0 else 0.0
 
 
 def run_reference(args, rank, world):
@@ -239,6 +252,7 @@ def run_reference(args, rank, world):
     sample = OracleSample(workloads.llama1b(args.history))
     for k in range(args.warmup):
         sample.run(0.0, 1, first=k)
+    sample.cpu_s = sample.wall_s = 0.0
     times, nbytes = [], 0
     for k in range(args.steps):
         t, nb, _ = sample.run(0.0, 1, first=k)
@@ -254,6 +268,7 @@ def run_reference(args, rank, world):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(args, world),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "cpu_time_over_wall": sample.cpu_per_wall(),
                          "sample": f"each step: the fp64 oracle over 1 of the 64 sequences "
                                    f"(history {args.history}, all 32 query heads)"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -523,9 +538,11 @@ def main():
         line["chunk"] = chunk(pa, workloads, torch, dev, peak)
         line["prefill"] = prefill(pa, workloads, torch, dev)
         if world == 1:
-            t, nb, n = OracleSample(cpu).run(12.0, 64)
+            sample = OracleSample(cpu)
+            t, nb, n = sample.run(12.0, 64)
             line["cpu_baseline"] = {
                 "value": nb / t / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+                "cpu_time_over_wall": sample.cpu_per_wall(),
                 "sample": f"{n} whole sequences of the headline batch (history {args.history}, "
                           f"32 query heads each), fp64 NumPy, one thread"}
     if rank == 0:

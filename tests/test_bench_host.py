@@ -6,6 +6,7 @@ import json
 import os
 import sys
 import tempfile
+import time
 
 import pytest
 
@@ -95,3 +96,19 @@ def test_clock_sampler_without_nvidia_smi(monkeypatch, tmp_path):
     s = bench.ClockSampler(0)
     s.start()
     assert s.stop()["reasons"] == ["nvidia-smi unavailable"]
+
+
+def test_oracle_sample_counts_bytes_and_runs_on_one_thread():
+    import workloads
+    assert os.environ["OPENBLAS_NUM_THREADS"] == "1"   # set by bench before NumPy loads
+    batch = workloads.make_batch("cpu_sample", 40, "bf16", [300, 50, 4096], 32, 8, 64, 16, 300)
+    sample = bench.OracleSample(batch)
+    t, nb, n = sample.run(60.0, 2, first=1)
+    assert n == 2 and t > 0
+    assert nb == bench.read_bytes([50], 32, 8, 64, 2, 16) + bench.read_bytes([4096], 32, 8, 64, 2,
+                                                                             16)
+    # the ratio over a longer run, once the threads of the batch draw have gone idle
+    sample.cpu_s = sample.wall_s = 0.0
+    time.sleep(0.2)
+    sample.run(60.0, 6, first=2)
+    assert 0 < sample.cpu_per_wall() <= 1.5
