@@ -531,12 +531,17 @@ def main():
     }
 
     if rank == 0 and not args.no_extras:
-        line["sweep"] = sweep(pa, workloads, torch, dev, flush, peak)
-        line["longctx"] = longctx(pa, workloads, torch, dev, peak)
-        line["ragged8b"] = ragged(pa, workloads, torch, dev, peak)
-        line["dense_vs_sdpa"] = dense_vs_sdpa(pa, workloads, torch, dev, peak)
-        line["chunk"] = chunk(pa, workloads, torch, dev, peak)
-        line["prefill"] = prefill(pa, workloads, torch, dev)
+        extras = (("sweep", lambda: sweep(pa, workloads, torch, dev, flush, peak)),
+                  ("longctx", lambda: longctx(pa, workloads, torch, dev, peak)),
+                  ("ragged8b", lambda: ragged(pa, workloads, torch, dev, peak)),
+                  ("dense_vs_sdpa", lambda: dense_vs_sdpa(pa, workloads, torch, dev, peak)),
+                  ("chunk", lambda: chunk(pa, workloads, torch, dev, peak)),
+                  ("prefill", lambda: prefill(pa, workloads, torch, dev)))
+        for key, run_extra in extras:
+            try:
+                line[key] = run_extra()
+            except Exception as e:  # the headline stands; the failure is reported in its place
+                line[key] = {"error": f"{type(e).__name__}: {e}"}
         if world == 1:
             sample = OracleSample(cpu)
             t, nb, n = sample.run(12.0, 64)
