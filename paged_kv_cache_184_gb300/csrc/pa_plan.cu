@@ -47,6 +47,8 @@ extern "C" int32_t pa_plan_work(const int32_t *seq_lens, int32_t num_seqs, int32
     // as many items as fit whole: each at least item_pages, below 2 * item_pages
     const int64_t n = std::max<int64_t>(1, pages[b] / item_pages);
     if (n > 32767) return -1;  // the slot count must fit 15 bits of the item record
+    // refuse a plan that outgrows the caller's buffer before building it
+    if (static_cast<int64_t>(list.size()) + n > max_items) return -1;
     slots = std::max<int32_t>(slots, static_cast<int32_t>(n));
     // n near-equal page runs covering the sequence in order
     for (int64_t j = 0; j < n; ++j) {
@@ -57,7 +59,6 @@ extern "C" int32_t pa_plan_work(const int32_t *seq_lens, int32_t num_seqs, int32
                       static_cast<int32_t>(j), static_cast<int32_t>(n)});
     }
   }
-  if (static_cast<int64_t>(list.size()) > max_items) return -1;
   // longest first, so the shortest items fill the end of the grid
   std::stable_sort(list.begin(), list.end(), [](const Item &x, const Item &y) {
     return (x.end - x.begin) > (y.end - y.begin);

@@ -80,3 +80,20 @@ def test_plan_refuses_a_small_buffer_and_negative_lengths(lib):
                                   ctypes.addressof(items), 2, ctypes.byref(slots)) == -1
     assert lib.raw().pa_plan_work(ctypes.addressof(lens), 3, 8, 16, 100, 1,
                                   ctypes.addressof(items), 2, ctypes.byref(slots)) == -1
+
+
+def test_plan_fits_a_buffer_of_exactly_its_size(lib):
+    lens_list = [16, 5000, 3000, 12000, 1, 700]
+    lens = (ctypes.c_int32 * len(lens_list))(*lens_list)
+
+    def plan(max_items):
+        items = (ctypes.c_int32 * (4 * 1000))()
+        slots = ctypes.c_int32(0)
+        n = lib.raw().pa_plan_work(ctypes.addressof(lens), len(lens_list), 8, 16, 600, 1,
+                                   ctypes.addressof(items), max_items, ctypes.byref(slots))
+        return n, list(items)[:4 * max(n, 0)], slots.value
+
+    n, items, slots = plan(1000)
+    assert n > len(lens_list)                      # the long sequences are cut
+    assert plan(n) == (n, items, slots)            # the same plan in a buffer of n items
+    assert plan(n - 1)[0] == -1
