@@ -191,8 +191,9 @@ pa_status pa_merge(void *out, const float *partial_out,
  * item's index within its sequence.  Writes at most max_items items to
  * `items` (host memory, [max_items][4]) and the largest per-sequence item
  * count to *max_slots.  Returns the number of items, or -1 for bad
- * arguments or too small a buffer (num_seqs + total pages / min pages
- * always suffices).
+ * arguments, too small a buffer (num_seqs + total pages / min pages
+ * always suffices) or a sequence that would need more than 32767 items
+ * (the slot field's 15 bits); the buffer is left unwritten then.
  */
 int32_t pa_plan_work(const int32_t *seq_lens, int32_t num_seqs, int32_t num_kv_heads,
                      int32_t block_size, int32_t target_ctas, int32_t min_pages_per_item,
