@@ -251,6 +251,32 @@ def test_large_scores_stay_finite():
     np.testing.assert_allclose(out[..., :4], base, rtol=0, atol=1e-9)
 
 
+def test_peaky_key_dominates_within_the_softmax_bound():
+    # one key row scaled x8 (the long-context workload's peaky keys): when its score leads
+    # every other by delta, the output is v of that token up to the weight the rest keep,
+    #   |out - v_top| <= r * max_t |v_t - v_top| / (1 + r),  r = (n - 1) exp(-delta)
+    rng = np.random.default_rng(31)
+    n, d, ps = 40, 16, 4
+    k = rng.standard_normal((n // ps, ps, 1, d)) * 0.3
+    v = rng.standard_normal((n // ps, ps, 1, d))
+    q = rng.standard_normal((1, 1, d))
+    top = 23                                     # token 23: page 5, slot 3 (identity table)
+    k[top // ps, top % ps, 0] = 8.0 * q[0, 0] / np.linalg.norm(q[0, 0])
+    bt = np.arange(n // ps)[None, :]
+    scale = 1.0 / math.sqrt(d)
+    out = oracle.paged_decode(q, k, v, bt, np.array([n]), scale, ps)[0, 0]
+    kh = k.reshape(n, d)
+    vh = v.reshape(n, d)
+    s = scale * (kh @ q[0, 0])
+    delta = s[top] - np.max(np.delete(s, top))
+    assert delta > 1.0                           # the scaled key does lead
+    r = (n - 1) * math.exp(-delta)
+    bound = r * np.max(np.abs(vh - vh[top])) / (1 + r)
+    assert np.max(np.abs(out - vh[top])) <= bound + 1e-12
+    # and it is no closed form by accident: the other tokens still move the output
+    assert np.max(np.abs(out - vh[top])) > 0
+
+
 # --------------------------------------------------------------------------
 # invariants
 
