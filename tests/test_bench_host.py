@@ -112,3 +112,36 @@ def test_oracle_sample_counts_bytes_and_runs_on_one_thread():
     time.sleep(0.2)
     sample.run(60.0, 6, first=2)
     assert 0 < sample.cpu_per_wall() <= 1.5
+
+
+class _ScriptedClock:
+    """Stands in for the time module: each perf_counter() call is one second after the
+    last; process_time() advances 2.5 s per call."""
+
+    def __init__(self):
+        self.wall = -1.0
+        self.cpu = -2.5
+
+    def perf_counter(self):
+        self.wall += 1.0
+        return self.wall
+
+    def process_time(self):
+        self.cpu += 2.5
+        return self.cpu
+
+
+def test_oracle_sample_stops_at_its_budget_on_a_scripted_clock(monkeypatch):
+    import workloads
+    batch = workloads.make_batch("clock", 41, "f32", [20, 9, 33, 5], 4, 2, 8, 4, 40)
+    sample = bench.OracleSample(batch)
+    monkeypatch.setattr(bench, "time", _ScriptedClock())
+    # start at 0; the budget check after sequences 1, 2, 3 reads 1, 2, 3 s: 3 > 2.5 stops it,
+    # and the final reading (4 s) is the wall time returned
+    t, nb, n = sample.run(2.5, 64, first=1)
+    assert (t, n) == (4.0, 3)
+    assert nb == sum(bench.read_bytes([x], 4, 2, 8, 4, 4) for x in (9, 33, 5))
+    assert sample.cpu_per_wall() == pytest.approx(2.5 / 4.0, abs=0.01)   # rounded to 0.01
+    # a count limit ends the run before the budget does
+    t, nb, n = sample.run(100.0, 2, first=0)
+    assert n == 2 and nb == sum(bench.read_bytes([x], 4, 2, 8, 4, 4) for x in (20, 9))
