@@ -38,9 +38,10 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-# The CPU baseline is the oracle on one thread: hold NumPy's BLAS to one thread
-# as well (read when NumPy loads, which happens after this point).
-os.environ["OPENBLAS_NUM_THREADS"] = "1"
+if __name__ == "__main__":
+    # The CPU baseline is the oracle on one thread: hold NumPy's BLAS to one
+    # thread as well (read when NumPy loads, which happens after this point).
+    os.environ["OPENBLAS_NUM_THREADS"] = "1"
 
 METRIC = "paged decode attention: achieved HBM GB/s (% of GB300 peak), µs/step at B=64"
 UNIT = "GB/s"
@@ -269,6 +270,7 @@ def run_reference(args, rank, world):
         "config": workload_config(args, world),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "cpu_time_over_wall": sample.cpu_per_wall(),
+                         "blas_threads": os.environ.get("OPENBLAS_NUM_THREADS"),
                          "sample": f"each step: the fp64 oracle over 1 of the 64 sequences "
                                    f"(history {args.history}, all 32 query heads)"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -548,6 +550,7 @@ def main():
             line["cpu_baseline"] = {
                 "value": nb / t / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
                 "cpu_time_over_wall": sample.cpu_per_wall(),
+                "blas_threads": os.environ.get("OPENBLAS_NUM_THREADS"),
                 "sample": f"{n} whole sequences of the headline batch (history {args.history}, "
                           f"32 query heads each), fp64 NumPy, one thread"}
     if rank == 0:

@@ -75,3 +75,4 @@ def test_reference_arm_under_torchrun_prints_one_line_from_rank_0(tmp_path):
     j = json.loads(lines[0])
     assert j["impl"] == "reference" and j["n_gpus"] == 2 and j["value"] > 0
     assert j["cpu_baseline"]["cores"] == 1 and 0 < j["cpu_baseline"]["cpu_time_over_wall"] <= 1.5
+    assert j["cpu_baseline"]["blas_threads"] == "1"      # pinned when bench.py runs as a script
