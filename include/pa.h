@@ -21,9 +21,14 @@
  *
  * Ownership: every pointer is device memory owned by the caller.  The
  * library allocates no memory and launches its kernels asynchronously on the
- * caller's stream; the call returns once the launch is queued.  Apart from
- * the fixed array behind pa_decode_splitkv_noalloc it keeps no state between
- * calls.
+ * caller's stream; the call returns once the launch is queued.  Between
+ * calls it keeps only host-side facts looked up once per CUDA context (each
+ * kernel's shared-memory setting, the SM count and occupancy, recently
+ * encoded tensor maps of the pools, the device address of the array behind
+ * pa_decode_splitkv_noalloc) and that fixed array itself.  Cached facts are
+ * keyed by the driver's context id, which is unique for the life of the
+ * process, so they stay correct across a device reset or a change of
+ * context.
  *
  * Errors: argument checks run on the host before any launch and return
  * PA_ERR_INVALID_ARG (a null or misaligned pointer, a negative or
@@ -248,9 +253,8 @@ pa_status pa_decode_work(float *partial_out, float *partial_lse, const int32_t *
  *
  * The tcgen05 reads wait on mbarriers with a bound (about a second per wait);
  * a wait that runs out records PA_DEV_TIMEOUT in *dev_err, the affected
- * outputs are zeroed and the context stays usable.  Test hook: with the
- * environment variable PA_TEST_WITHHOLD_TILES=1 the warp-specialized read
- * (256+ rows per kv head) loads no key tile, so that path can be exercised.
+ * outputs are zeroed and the context stays usable (pa_test_set_withhold_tiles
+ * makes that happen on purpose).
  */
 pa_status pa_decode_chunk(void *out, const void *q, const void *k_pool,
                           const void *v_pool, const int32_t *block_table,
@@ -291,6 +295,16 @@ pa_status pa_decode_chunk_splitkv(float *partial_out, float *partial_lse, const 
                                   int32_t pages_per_split, int32_t max_splits, pa_dtype dtype,
                                   int32_t *dev_err, pa_stream_t stream);
 
+/*
+ * pa_test_set_withhold_tiles - test hook for the bounded waits (not for
+ * production use).  While on (nonzero), the warp-specialized tcgen05 chunk
+ * read (256 or more (query, head) rows per kv head) loads no key tile: its
+ * waits run out after about a second each, and the call records
+ * PA_DEV_TIMEOUT with zeroed outputs, with no copy or MMA in flight.  Off by
+ * default; process-wide; affects launches issued while it is on.
+ */
+void pa_test_set_withhold_tiles(int32_t on);
+
 /* Size of the library-owned partials array behind pa_decode_splitkv_noalloc. */
 #define PA_NOALLOC_SCRATCH_BYTES (32u << 20)
 
@@ -312,10 +326,14 @@ pa_status pa_decode_chunk_splitkv(float *partial_out, float *partial_lse, const 
  * Limit: the partials take num_seqs * num_q_heads * splits * (head_dim + 1)
  * floats (each part rounded up to 256 bytes).  A call that needs more than
  * PA_NOALLOC_SCRATCH_BYTES returns PA_ERR_UNSUPPORTED and launches nothing.
- * Other arguments are checked as in pa_decode_splitkv and pa_merge.
+ * Arguments are checked first as in pa_decode_splitkv (same status for the
+ * same arguments), then the limit, then out (non-null, 16-byte aligned).
  *
- * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
+ * The array's device address belongs to the CUDA context the library's
+ * module was loaded into.  The first call in a context (the first on a
+ * device, and the first after a device reset or in another context) looks it
+ * up with cudaGetSymbolAddress, with that context current; later calls in
+ * the same context reuse it.  Make that first call before any stream
  * capture.  Call it with the device that owns the stream and the data
  * current.  Every call on a device shares the one array.  Nothing depends on
  * what an earlier call left there, but calls whose kernels overlap on the GPU

@@ -8,7 +8,8 @@ no other implementation to fall back on, so a missing library raises.
 
 The names match the C ABI: pa_cache_append, pa_decode, pa_decode_splitkv,
 pa_merge, pa_decode_chunk, pa_decode_chunk_splitkv, pa_plan_work, pa_decode_work,
-pa_decode_splitkv_noalloc, pa_num_splits, pa_status_string, pa_version.
+pa_decode_splitkv_noalloc, pa_num_splits, pa_status_string, pa_version, and the
+test hook pa_test_set_withhold_tiles.
 """
 
 from __future__ import annotations
@@ -28,7 +29,8 @@ PA_DEV_BAD_ITEM, PA_DEV_TIMEOUT = 5, 6
 
 EXPORTED = ("pa_status_string", "pa_version", "pa_num_splits", "pa_cache_append",
             "pa_decode", "pa_decode_splitkv", "pa_merge", "pa_decode_splitkv_noalloc",
-            "pa_decode_chunk", "pa_decode_chunk_splitkv", "pa_plan_work", "pa_decode_work")
+            "pa_decode_chunk", "pa_decode_chunk_splitkv", "pa_plan_work", "pa_decode_work",
+            "pa_test_set_withhold_tiles")
 
 # bytes of the library-owned partials array behind pa_decode_splitkv_noalloc
 PA_NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -59,6 +61,7 @@ _SIGNATURES = {
                                                _i, _i, _f, _i, _i, ctypes.c_int, _p, _p]),
     "pa_decode_splitkv_noalloc": (ctypes.c_int, [_p, _p, _p, _p, _p, _i, _p, _i, _i, _i, _i, _i,
                                                  _i, _f, _i, ctypes.c_int, _p, _p]),
+    "pa_test_set_withhold_tiles": (None, [_i]),
 }
 
 
@@ -122,6 +125,17 @@ def _stream(stream) -> Optional[int]:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
+def _check_batch(fn: str, b: int, block_table, seq_lens) -> None:
+    """The table and the lengths must have exactly one row per sequence of the batch:
+    the C ABI carries no row count for them, so a short tensor would be read past
+    its end."""
+    if block_table.dim() != 2 or block_table.shape[0] != b:
+        raise ValueError(f"{fn}: block_table must be [{b}, max_blocks], got "
+                         f"{list(block_table.shape)}")
+    if seq_lens.dim() != 1 or seq_lens.shape[0] != b:
+        raise ValueError(f"{fn}: seq_lens must be [{b}], got {list(seq_lens.shape)}")
+
+
 def _check(fn: str, status: int) -> None:
     if status != PA_OK:
         raise PaError(fn, status)
@@ -139,6 +153,12 @@ def pa_num_splits(max_blocks_per_seq: int, pages_per_split: int) -> int:
     return int(load().pa_num_splits(max_blocks_per_seq, pages_per_split))
 
 
+def pa_test_set_withhold_tiles(on: bool) -> None:
+    """Test hook: while on, the warp-specialized chunk read loads no key tile and its
+    bounded waits run out (PA_DEV_TIMEOUT, zeroed outputs)."""
+    load().pa_test_set_withhold_tiles(1 if on else 0)
+
+
 def pa_cache_append(k_new, v_new, k_pool, v_pool, block_table, positions, seq_ids=None,
                     dev_err=None, stream=None) -> None:
     """Scatter k_new/v_new [T, Hkv, d] into their page slots of k_pool/v_pool."""
@@ -147,6 +167,16 @@ def pa_cache_append(k_new, v_new, k_pool, v_pool, block_table, positions, seq_id
     num_pages, block_size, hkv, d = k_pool.shape
     if v_pool.shape != k_pool.shape or k_new.shape != v_new.shape or k_new.shape[1:] != (hkv, d):
         raise ValueError("pa_cache_append: inconsistent K/V shapes")
+    t = k_new.shape[0]
+    if block_table.dim() != 2:
+        raise ValueError("pa_cache_append: block_table must be [num_seqs, max_blocks]")
+    if positions.dim() != 1 or positions.shape[0] != t:
+        raise ValueError(f"pa_cache_append: positions must be [{t}], got {list(positions.shape)}")
+    if seq_ids is not None and (seq_ids.dim() != 1 or seq_ids.shape[0] != t):
+        raise ValueError(f"pa_cache_append: seq_ids must be [{t}], got {list(seq_ids.shape)}")
+    if seq_ids is None and t > block_table.shape[0]:
+        raise ValueError("pa_cache_append: without seq_ids token i belongs to sequence i, so "
+                         "the table needs a row per token")
     dt = k_pool.dtype
     st = lib.pa_cache_append(
         _ptr(k_new, "k_new", dt), _ptr(v_new, "v_new", dt), _ptr(k_pool, "k_pool", dt),
@@ -168,6 +198,7 @@ def pa_decode(out, q, k_pool, v_pool, block_table, seq_lens, scale: float, dev_e
     b, hq, dq = q.shape
     if dq != d or out.shape != q.shape or v_pool.shape != k_pool.shape:
         raise ValueError("pa_decode: inconsistent shapes")
+    _check_batch("pa_decode", b, block_table, seq_lens)
     dt = q.dtype
     st = lib.pa_decode(
         _ptr(out, "out", dt), _ptr(q, "q", dt), _ptr(k_pool, "k_pool", dt),
@@ -188,6 +219,9 @@ def pa_decode_splitkv(partial_out, partial_lse, q, k_pool, v_pool, block_table, 
     max_splits = partial_lse.shape[2]
     if partial_out.shape != (b, hq, max_splits, d) or partial_lse.shape != (b, hq, max_splits):
         raise ValueError("pa_decode_splitkv: partial shapes must be [B,Hq,S,d] and [B,Hq,S]")
+    if v_pool.shape != k_pool.shape:
+        raise ValueError("pa_decode_splitkv: inconsistent shapes")
+    _check_batch("pa_decode_splitkv", b, block_table, seq_lens)
     dt = q.dtype
     st = lib.pa_decode_splitkv(
         _ptr(partial_out, "partial_out", torch.float32),
@@ -209,6 +243,7 @@ def pa_decode_chunk(out, q, k_pool, v_pool, block_table, seq_lens, scale: float,
     b, nq, hq, dq = q.shape
     if dq != d or out.shape != q.shape or v_pool.shape != k_pool.shape:
         raise ValueError("pa_decode_chunk: inconsistent shapes")
+    _check_batch("pa_decode_chunk", b, block_table, seq_lens)
     dt = q.dtype
     st = lib.pa_decode_chunk(
         _ptr(out, "out", dt), _ptr(q, "q", dt), _ptr(k_pool, "k_pool", dt),
@@ -236,6 +271,7 @@ def pa_decode_chunk_splitkv(partial_out, partial_lse, q, k_pool, v_pool, block_t
             partial_lse.shape != (b, nq, hq, max_splits)):
         raise ValueError("pa_decode_chunk_splitkv: partial shapes must be [B,n_q,Hq,S,d] and "
                          "[B,n_q,Hq,S]")
+    _check_batch("pa_decode_chunk_splitkv", b, block_table, seq_lens)
     dt = q.dtype
     st = lib.pa_decode_chunk_splitkv(
         _ptr(partial_out, "partial_out", torch.float32),
@@ -271,8 +307,13 @@ def pa_plan_work(seq_lens, num_kv_heads: int, block_size: int, target_ctas: int,
 
 
 def pa_decode_work(partial_out, partial_lse, items, q, k_pool, v_pool, block_table, seq_lens,
-                   scale: float, dev_err=None, stream=None) -> None:
-    """Split read over a planned work list (items: device int32 [n, 4] from pa_plan_work)."""
+                   scale: float, dev_err=None, stream=None, items_host=None) -> None:
+    """Split read over a planned work list (items: device int32 [n, 4] from pa_plan_work).
+
+    items_host, the plan's host copy when the caller still has it, is checked
+    against the batch before the launch: same shape, sequence ids in [0, B) and
+    slots below max_slots.
+    """
     import torch
     lib = load()
     num_pages, block_size, hkv, d = k_pool.shape
@@ -282,6 +323,19 @@ def pa_decode_work(partial_out, partial_lse, items, q, k_pool, v_pool, block_tab
         raise ValueError("pa_decode_work: partial shapes must be [B,Hq,S,d] and [B,Hq,S]")
     if items.dim() != 2 or items.shape[1] != 4:
         raise ValueError("pa_decode_work: items must be [n, 4]")
+    if v_pool.shape != k_pool.shape:
+        raise ValueError("pa_decode_work: inconsistent shapes")
+    _check_batch("pa_decode_work", b, block_table, seq_lens)
+    if items_host is not None:
+        h = torch.as_tensor(items_host)
+        if tuple(h.shape) != tuple(items.shape):
+            raise ValueError("pa_decode_work: items_host and items differ in shape")
+        if h.numel():
+            seq, slot, count = h[:, 0], h[:, 3] & 0xFFFF, h[:, 3] >> 16
+            if bool(((seq < 0) | (seq >= b)).any()):
+                raise ValueError(f"pa_decode_work: an item names a sequence outside [0, {b})")
+            if bool(((slot >= count) | (count > max_slots)).any()):
+                raise ValueError("pa_decode_work: an item's slot or count exceeds max_slots")
     dt = q.dtype
     st = lib.pa_decode_work(
         _ptr(partial_out, "partial_out", torch.float32),
@@ -333,6 +387,7 @@ def pa_decode_splitkv_noalloc(out, q, k_pool, v_pool, block_table, seq_lens, sca
     b, hq, dq = q.shape
     if dq != d or out.shape != q.shape or v_pool.shape != k_pool.shape:
         raise ValueError("pa_decode_splitkv_noalloc: inconsistent shapes")
+    _check_batch("pa_decode_splitkv_noalloc", b, block_table, seq_lens)
     dt = q.dtype
     st = lib.pa_decode_splitkv_noalloc(
         _ptr(out, "out", dt), _ptr(q, "q", dt), _ptr(k_pool, "k_pool", dt),

@@ -39,8 +39,10 @@ int log2_exact(int32_t x) {  // -1 unless x is a power of two
   return r;
 }
 
+}  // namespace
+
 // Checks shared by the reads: shapes, dtype, head dim, group, block size.
-pa_status check_read_shape(int32_t max_blocks, int32_t num_seqs, int32_t hq, int32_t hkv,
+pa_status pa::check_read_shape(int32_t max_blocks, int32_t num_seqs, int32_t hq, int32_t hkv,
                            int32_t d, int32_t block_size, int32_t num_pages, float scale,
                            pa_dtype dtype) {
   if (max_blocks <= 0 || num_seqs < 0 || hq <= 0 || hkv <= 0 || d <= 0 || num_pages <= 0)
@@ -60,6 +62,10 @@ pa_status check_read_shape(int32_t max_blocks, int32_t num_seqs, int32_t hq, int
   // a page count times rows must fit the int64 row index (always true here)
   return PA_OK;
 }
+
+namespace {
+
+using pa::check_read_shape;
 
 pa::DecodeParams make_params(const void *q, const void *k_pool, const void *v_pool,
                              const int32_t *block_table, int32_t max_blocks,

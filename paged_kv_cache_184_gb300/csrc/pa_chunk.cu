@@ -375,7 +375,7 @@ template <typename T, int D>
 cudaError_t launch_d(const ChunkParams &p, cudaStream_t stream) {
   auto kern = chunk_kernel<T, D>;
   const int smem = ChunkShape<D>::kSmemBytes;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t err = set_max_smem(reinterpret_cast<const void *>(kern), smem);
   if (err != cudaSuccess) return err;
   const int rblocks = (p.chunk_len * p.group + kRowsPerCta - 1) / kRowsPerCta;
   dim3 grid(rblocks * p.num_kv_heads, p.num_seqs, p.partial_out ? p.num_splits : 1);

@@ -330,7 +330,7 @@ template <typename T, int D>
 cudaError_t launch_d(const ChunkParams &p, cudaStream_t stream) {
   auto kern = chunk_tc_kernel<T, D>;
   const int smem = TcShape<D>::kSmem;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t err = set_max_smem(reinterpret_cast<const void *>(kern), smem);
   if (err != cudaSuccess) return err;
   const int nblk = (p.chunk_len * p.group + kRows - 1) / kRows;
   dim3 grid(nblk * p.num_kv_heads, p.num_seqs, p.partial_out ? p.num_splits : 1);

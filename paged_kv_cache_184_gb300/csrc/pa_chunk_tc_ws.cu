@@ -42,7 +42,7 @@
 #include <cuda.h>  // CUtensorMap (the encoder is fetched through the runtime)
 #include <math_constants.h>
 
-#include <cstdlib>
+#include <atomic>
 #include <mutex>
 
 #include "pa_common.cuh"
@@ -616,23 +616,61 @@ bool make_pool_map(CUtensorMap *map, const void *pool, pa_dtype dtype, const Chu
   return r == CUDA_SUCCESS;
 }
 
+// Recently encoded pool maps, so that a serving loop calling with the same
+// pools encodes each map once.  A map is a pure function of its arguments
+// (the pool's address, extents and dtype), valid in any context.
+struct MapKey {
+  const void *pool;
+  int32_t num_pages, block_size_log2, num_kv_heads, head_dim;
+  pa_dtype dtype;
+  bool operator==(const MapKey &o) const {
+    return pool == o.pool && num_pages == o.num_pages && block_size_log2 == o.block_size_log2 &&
+           num_kv_heads == o.num_kv_heads && head_dim == o.head_dim && dtype == o.dtype;
+  }
+};
+constexpr int kMapCache = 16;
+std::mutex g_map_mu;
+MapKey g_map_key[kMapCache];
+CUtensorMap g_map_val[kMapCache];
+int g_map_used = 0, g_map_next = 0;
+
+bool pool_map(CUtensorMap *map, const void *pool, pa_dtype dtype, const ChunkParams &p) {
+  const MapKey key{pool, p.num_pages, p.block_size_log2, p.num_kv_heads, p.head_dim, dtype};
+  {
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    for (int i = 0; i < g_map_used; ++i)
+      if (g_map_key[i] == key) {
+        *map = g_map_val[i];
+        return true;
+      }
+  }
+  if (!make_pool_map(map, pool, dtype, p)) return false;
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  const int i = g_map_used < kMapCache ? g_map_used++ : (g_map_next++ % kMapCache);
+  g_map_key[i] = key;
+  g_map_val[i] = *map;
+  return true;
+}
+
+// Test hook for the time-out path (set through pa_test_set_withhold_tiles):
+// the load warps announce no tile, every wait then runs out (after about a
+// second of the global timer, or 2^26 polls) and the call reports
+// PA_DEV_TIMEOUT with zeroed outputs.  Nothing is in flight when the waits
+// give up.  Off unless a test turns it on.
+std::atomic<int> g_withhold_tiles{0};
+
 template <typename T, int D>
 cudaError_t launch_d(const ChunkParams &p, pa_dtype dtype, cudaStream_t stream) {
   auto kern = chunk_tc_ws_kernel<T, D>;
   const int smem = WsShape<D>::kSmem;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t err = set_max_smem(reinterpret_cast<const void *>(kern), smem);
   if (err != cudaSuccess) return err;
   // tensor-map copies need pages of at least 8 tokens (a 1024-byte swizzle
   // atom per copy); otherwise, or without an encoder, every tile uses cp.async
   CUtensorMap mk{}, mv{};
-  const int use_tma = p.block_size_log2 >= 3 && make_pool_map(&mk, p.k_pool, dtype, p) &&
-                      make_pool_map(&mv, p.v_pool, dtype, p);
-  // Test hook for the time-out path: PA_TEST_WITHHOLD_TILES=1 makes the load
-  // warps announce no tile; every wait then runs out (after about a second of
-  // the global timer, or 2^26 polls) and the call reports PA_DEV_TIMEOUT with
-  // zeroed outputs.  Nothing is in flight when the waits give up.
-  const char *hold = std::getenv("PA_TEST_WITHHOLD_TILES");
-  const int withhold = hold != nullptr && hold[0] == '1' && hold[1] == '\0';
+  const int use_tma = p.block_size_log2 >= 3 && pool_map(&mk, p.k_pool, dtype, p) &&
+                      pool_map(&mv, p.v_pool, dtype, p);
+  const int withhold = g_withhold_tiles.load(std::memory_order_relaxed);
   const int nblk = (p.chunk_len * p.group + kCtaRows - 1) / kCtaRows;
   dim3 grid(nblk * p.num_kv_heads, p.num_seqs, p.partial_out ? p.num_splits : 1);
   return launch_pdl(kern, grid, dim3(kThreads), smem, stream, p, mk, mv, use_tma, withhold);
@@ -662,3 +700,7 @@ cudaError_t launch_chunk_tc_ws(const ChunkParams &p, pa_dtype dtype, cudaStream_
 }
 
 }  // namespace pa
+
+extern "C" void pa_test_set_withhold_tiles(int32_t on) {
+  pa::g_withhold_tiles.store(on != 0 ? 1 : 0, std::memory_order_relaxed);
+}

@@ -608,15 +608,11 @@ cudaError_t launch_shape(DecodeParams p, cudaStream_t stream) {
     // make the grid fit the resident slots.
     const int ch = p.group <= 4 ? 4 : S::kHeads;
     const int smem_multi = S::kRingBytes + kWarps * ch * (D + 2) * 4;
-    int dev = 0, sms = 0, per_sm = 0;
-    cudaError_t err = cudaGetDevice(&dev);
-    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int sms = 0, per_sm = 0;
+    cudaError_t err = sm_count(&sms);
     if (err == cudaSuccess)
-      err = cudaFuncSetAttribute(kern_multi, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 smem_multi);
-    if (err == cudaSuccess)
-      err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern_multi, kThreads,
-                                                          smem_multi);
+      err = blocks_per_sm(&per_sm, reinterpret_cast<const void *>(kern_multi), kThreads,
+                          smem_multi);
     if (err != cudaSuccess) return err;
     const long long pairs = static_cast<long long>(p.num_seqs) * p.num_kv_heads;
     const long long slots = static_cast<long long>(sms) * per_sm;
@@ -633,7 +629,7 @@ cudaError_t launch_shape(DecodeParams p, cudaStream_t stream) {
   const int groups = (p.num_splits + p.splits_per_cta - 1) / p.splits_per_cta;
   dim3 grid(groups * p.num_kv_heads, p.num_seqs);
   if (p.splits_per_cta > 1) return launch_pdl(kern_multi, grid, dim3(kThreads), smem, stream, p);
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t err = set_max_smem(reinterpret_cast<const void *>(kern), smem);
   if (err != cudaSuccess) return err;
   return launch_pdl(kern, grid, dim3(kThreads), smem, stream, p);
 }
@@ -642,8 +638,7 @@ template <typename T, int D, int NT>
 cudaError_t launch_items_shape(const DecodeParams &p, cudaStream_t stream) {
   using S = Shape<D, NT>;
   auto kern = decode_mma_kernel<T, D, NT, false, true, false>;
-  cudaError_t err =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+  cudaError_t err = set_max_smem(reinterpret_cast<const void *>(kern), S::kSmemBytes);
   if (err != cudaSuccess) return err;
   dim3 grid(p.num_items * p.num_kv_heads, 1);
   return launch_pdl(kern, grid, dim3(kThreads), S::kSmemBytes, stream, p);

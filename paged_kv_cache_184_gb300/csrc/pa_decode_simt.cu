@@ -308,8 +308,7 @@ cudaError_t launch_shape(const DecodeParams &p, int nch, int tg_log2, cudaStream
   const size_t combine = static_cast<size_t>(ng) * GMAX * (2 + p.head_dim) * sizeof(float);
   const size_t smem = ring > combine ? ring : combine;
   auto kern = decode_simt_kernel<T, GMAX, CPL>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+  cudaError_t err = set_max_smem(reinterpret_cast<const void *>(kern), static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   dim3 grid(p.num_splits * p.num_kv_heads, p.num_seqs);
   kern<<<grid, kThreads, smem, stream>>>(p, nch, tg_log2);

@@ -31,6 +31,24 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Per-context host cache (pa_host.cu).  Each fact is looked up once per CUDA
+// context (keyed by the driver's process-unique context id), so a launch
+// repeats no runtime query; with no current context the query runs uncached.
+uint64_t current_context_id();  // 0 when no context is current or it has no id
+// cudaFuncSetAttribute(kern, MaxDynamicSharedMemorySize, smem), once per context.
+cudaError_t set_max_smem(const void *kern, int smem);
+// Streaming multiprocessors of the current device.
+cudaError_t sm_count(int *sms);
+// Resident CTAs per SM of `kern` at `threads` threads and `smem` dynamic shared
+// bytes (also sets the kernel's shared-memory limit to smem).
+cudaError_t blocks_per_sm(int *n, const void *kern, int threads, int smem);
+
+// Shape checks shared by every read entry point (pa_api.cu): sizes, dtype,
+// head dim, group and block size, before any pointer is looked at.
+pa_status check_read_shape(int32_t max_blocks, int32_t num_seqs, int32_t hq, int32_t hkv,
+                           int32_t d, int32_t block_size, int32_t num_pages, float scale,
+                           pa_dtype dtype);
+
 // Arguments of one paged read (pa_decode or pa_decode_splitkv).
 struct DecodeParams {
   void *out;            // [B][Hq][D] dtype; unused by the split-KV read

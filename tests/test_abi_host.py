@@ -205,12 +205,35 @@ def test_binding_raises_on_bad_status(lib):
     assert "PA_ERR_UNSUPPORTED" in str(pa.PaError("pa_decode", 2))
 
 
+# 53 sequences x 5 heads x 487 splits = 129,055 partial rows: 256 x 129,055 bytes of outputs
+# and 516,220 of lse rounded up to 516,352 fill the 32 MiB array exactly; 488 splits do not
+EXACT_FIT = dict(b=53, hq=5, hkv=1, d=64, mb=487, pps=1)
+
+
+def test_exact_fit_shape_fills_the_array():
+    rows = 53 * 5 * 487
+    align = lambda x: (x + 255) // 256 * 256
+    assert align(rows * 64 * 4) + align(rows * 4) == pa.PA_NOALLOC_SCRATCH_BYTES
+    rows += 53 * 5
+    assert align(rows * 64 * 4) + align(rows * 4) > pa.PA_NOALLOC_SCRATCH_BYTES
+
+
 @pytest.mark.parametrize("kw,want", [
     (dict(pps=0), pa.PA_ERR_INVALID_ARG),
     (dict(b=-1), pa.PA_ERR_INVALID_ARG),
     (dict(b=0), pa.PA_OK),
     # 64 x 32 x 8192 splits x 65 floats: far beyond the fixed partials array
     (dict(b=64, mb=8192, pps=1), pa.PA_ERR_UNSUPPORTED),
+    # the read's own checks come first, as in pa_decode_splitkv: an empty batch with a bad
+    # shape, and an oversized batch with a bad group, are both invalid arguments
+    (dict(b=0, hkv=0), pa.PA_ERR_INVALID_ARG),
+    (dict(b=0, bs=24), pa.PA_ERR_INVALID_ARG),
+    (dict(b=0, dt=9), pa.PA_ERR_INVALID_ARG),
+    (dict(b=64, mb=8192, pps=1, hq=9, hkv=2), pa.PA_ERR_INVALID_ARG),
+    (dict(b=0, d=512), pa.PA_ERR_UNSUPPORTED),
+    (dict(EXACT_FIT, mb=488), pa.PA_ERR_UNSUPPORTED),    # one split past the exact fit
+    (dict(out=None), pa.PA_ERR_INVALID_ARG),             # refused before anything launches
+    (dict(out=MISALIGNED), pa.PA_ERR_INVALID_ARG),
 ])
 def test_noalloc_validation_before_any_device_call(lib, kw, want):
     a = dict(out=FAKE, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, mb=10, sl=FAKE, b=2, hq=32, hkv=8, d=64,
@@ -307,3 +330,84 @@ def test_binding_merge_and_chunk_split_shape_checks(lib):
     with pytest.raises(ValueError):                # head_dim of q and the pools must agree
         lib.pa_decode_chunk_splitkv(po, pl, torch.zeros(2, 3, 4, 32, dtype=torch.bfloat16), kp,
                                     kp, bt, sl, 0.125, 1)
+
+
+# ---- the binding checks every row count the C ABI cannot see -------------------------
+
+
+def _cpu_batch(b=2, hq=8, hkv=2, d=64, mb=4, nq=None):
+    import torch
+    q = torch.zeros((b, hq, d) if nq is None else (b, nq, hq, d), dtype=torch.bfloat16)
+    kp = torch.zeros(16, 16, hkv, d, dtype=torch.bfloat16)
+    bt = torch.zeros(b, mb, dtype=torch.int32)
+    sl = torch.ones(b, dtype=torch.int32)
+    return q, kp, bt, sl
+
+
+@pytest.mark.parametrize("what", ["short_table", "long_table", "short_lens", "long_lens",
+                                  "flat_table"])
+def test_binding_checks_table_and_lens_rows_of_every_read(lib, what):
+    import torch
+
+    def bad(bt, sl):
+        if what == "short_table":
+            return bt[:1], sl, "block_table"
+        if what == "long_table":
+            return torch.zeros(3, 4, dtype=torch.int32), sl, "block_table"
+        if what == "short_lens":
+            return bt, sl[:1], "seq_lens"
+        if what == "long_lens":
+            return bt, torch.ones(3, dtype=torch.int32), "seq_lens"
+        return bt.reshape(-1), sl, "block_table"
+
+    q, kp, bt, sl = _cpu_batch()
+    bt, sl, name = bad(bt, sl)
+    po, pl = torch.zeros(2, 8, 4, 64), torch.zeros(2, 8, 4)
+    calls = {
+        "pa_decode": lambda: lib.pa_decode(torch.empty_like(q), q, kp, kp, bt, sl, 0.125),
+        "pa_decode_splitkv": lambda: lib.pa_decode_splitkv(po, pl, q, kp, kp, bt, sl, 0.125, 1),
+        "pa_decode_splitkv_noalloc": lambda: lib.pa_decode_splitkv_noalloc(
+            torch.empty_like(q), q, kp, kp, bt, sl, 0.125, 1),
+        "pa_decode_work": lambda: lib.pa_decode_work(
+            po, pl, torch.zeros(2, 4, dtype=torch.int32), q, kp, kp, bt, sl, 0.125),
+    }
+    qc, _, _, _ = _cpu_batch(nq=3)
+    poc, plc = torch.zeros(2, 3, 8, 4, 64), torch.zeros(2, 3, 8, 4)
+    calls["pa_decode_chunk"] = lambda: lib.pa_decode_chunk(torch.empty_like(qc), qc, kp, kp, bt,
+                                                           sl, 0.125)
+    calls["pa_decode_chunk_splitkv"] = lambda: lib.pa_decode_chunk_splitkv(
+        poc, plc, qc, kp, kp, bt, sl, 0.125, 1)
+    for fn, call in calls.items():
+        with pytest.raises(ValueError, match=f"{fn}: {name} must be"):
+            call()
+
+
+def test_binding_checks_append_rows(lib):
+    import torch
+    kp = torch.zeros(16, 16, 2, 64, dtype=torch.bfloat16)
+    kn = torch.zeros(3, 2, 64, dtype=torch.bfloat16)
+    bt = torch.zeros(3, 4, dtype=torch.int32)
+    pos = torch.zeros(3, dtype=torch.int32)
+    with pytest.raises(ValueError, match="positions must be"):
+        lib.pa_cache_append(kn, kn, kp, kp, bt, pos[:2])
+    with pytest.raises(ValueError, match="seq_ids must be"):
+        lib.pa_cache_append(kn, kn, kp, kp, bt, pos, seq_ids=torch.zeros(4, dtype=torch.int32))
+    with pytest.raises(ValueError, match="a row per token"):
+        lib.pa_cache_append(kn, kn, kp, kp, bt[:2], pos)
+    with pytest.raises(ValueError, match="block_table must be"):
+        lib.pa_cache_append(kn, kn, kp, kp, bt.reshape(-1), pos)
+
+
+@pytest.mark.parametrize("items,match", [
+    ([[2, 0, 16, 1 << 16], [0, 0, 16, 1 << 16]], "outside"),           # sequence 2 of 2
+    ([[-1, 0, 16, 1 << 16], [1, 0, 16, 1 << 16]], "outside"),
+    ([[0, 0, 16, (5 << 16) | 4], [1, 0, 16, 1 << 16]], "max_slots"),   # 5 slots of 4
+    ([[0, 0, 16, (1 << 16) | 1], [1, 0, 16, 1 << 16]], "max_slots"),   # slot 1 of 1
+])
+def test_binding_checks_work_items_on_their_host_copy(lib, items, match):
+    import torch
+    q, kp, bt, sl = _cpu_batch()
+    po, pl = torch.zeros(2, 8, 4, 64), torch.zeros(2, 8, 4)
+    host = torch.tensor(items, dtype=torch.int32)
+    with pytest.raises(ValueError, match=match):
+        lib.pa_decode_work(po, pl, host.clone(), q, kp, kp, bt, sl, 0.125, items_host=host)

@@ -144,3 +144,109 @@ def test_oracle_sample_stops_at_its_budget_on_a_scripted_clock(monkeypatch):
     # a count limit ends the run before the budget does
     t, nb, n = sample.run(100.0, 2, first=0)
     assert n == 2 and nb == sum(bench.read_bytes([x], 4, 2, 8, 4, 4) for x in (20, 9))
+
+
+# ---- the JSON line stays short enough to reach the end of a 1.5 KB log tail ------------
+
+X = 12345.678901234   # every float at its longest once rounded to 4 significant figures
+
+
+def _fake_measurements():
+    import argparse
+    args = argparse.Namespace(history=4096)
+    return {"value": X, "world": 1, "steps": 20, "warmup": 5, "ms_per_step": 0.08734879978,
+            "config": bench.workload_config(args, 1),
+            "clocks": {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "sm_min_mhz": 1987.5,
+                       "power_w_median": 402.365, "samples": 8,
+                       "reasons": ["sw_power_cap"]},
+            "e2e_value": X, "h2d": 459264, "d2h": 262144, "serial_value": X,
+            "gpu_launches": 40, "achieved": X, "peak": 6705.2, "peak_kind": "measured",
+            "traffic": 541237504.0, "rb": 537460992, "dec_ms": [0.0854799, 0.0838879, 0.08179]}
+
+
+def _fake_extras():
+    hs = (16, 64, 256, 1024, 4096)
+    sweep = [{"history": h, "us_median": X, "us_min": X, "gbs": X, "frac": 0.73456789}
+             for h in hs]
+    longctx = [{"history": h, "splits": h // 1024, "us_split_plus_merge": X, "gbs": X,
+                "frac": 0.9512345, "us_single_pass": X} for h in (32768, 131072)]
+    ragged = {"batch": 256, "kv_gb": 4.5, "us_single_pass": X, "gbs_single_pass": X,
+              "us_split64_plus_merge": X, "gbs_split64": X, "frac_best": 1.0312345,
+              "planned": [{"target_ctas": 152 * m, "items": 900, "max_slots": 4, "us": X + m,
+                           "plan_host_us": X, "gbs": X} for m in (3, 6, 12, 24)]}
+    chunk = {"llama1b_h4096": [{"n_q": n, "us": X, "gbs": X, "frac_hbm": 0.3648199,
+                                "tflops": X} for n in (1, 4, 16, 64)],
+             "longctx_h32768_split": [{"n_q": n, "splits": 32, "us_split_plus_merge": X,
+                                       "gbs": X, "frac_hbm": 0.6, "us_single_pass": X}
+                                      for n in (1, 4, 16)]}
+    prefill = [{"head_dim": d, "batch": 8, "prompt": 4096, "us": X, "tflops": X,
+                "peak_tflops": 1886.7, "peak_source": "measured", "frac_tensor": 0.3456789}
+               for d in (64, 128)]
+    dense = [{"n_ctx": n, "us_by_splits": {}, "best_splits": 16, "us_best": X, "us_sdpa": X,
+              "gbs_best": X, "gbs_sdpa": X, "sdpa_over_ours": 1.469240007}
+             for n in (1024, 2048, 4096, 8192, 16384)]
+    return {"chunk": bench.compact_chunk(chunk), "dense_vs_sdpa": bench.compact_dense(dense),
+            "sweep": bench.compact_sweep(sweep), "longctx": bench.compact_longctx(longctx),
+            "ragged8b": bench.compact_ragged(ragged), "prefill": bench.compact_prefill(prefill)}
+
+
+def _fake_cpu():
+    # the shape bench.cpu_baseline returns
+    return {"value": X, "unit": "GB/s", "cores": 16, "kind": "oracle",
+            "sample": "123 passes of the h4096 batch, 1 proc/core",
+            "best_ms": X, "median_ms": X, "busy": 15.87654, "single_core": X}
+
+
+def test_the_whole_line_fits_a_1500_byte_tail():
+    line = bench.compact_json(bench.compose_line(_fake_measurements(), _fake_extras(),
+                                                 _fake_cpu()))
+    assert len(line.encode()) <= 1500, len(line.encode())
+    parsed = json.loads(line)
+    # every key the contract asks for, and the graded extras ending the line
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "clocks", "e2e", "gpu_launches", "roofline", "cpu_baseline"):
+        assert key in parsed, key
+    for key in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
+        assert key in parsed["roofline"], key
+    for key in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step"):
+        assert key in parsed["e2e"], key
+    assert list(parsed)[-4:] == list(bench.GRADED)
+    assert parsed["sweep"]["h"] == [16, 64, 256, 1024, 4096]
+    assert parsed["value"] == 12350                       # 4 significant figures
+
+
+def test_a_failed_extra_keeps_the_line_short():
+    extras = _fake_extras()
+    try:
+        raise RuntimeError("x" * 5000)
+    except RuntimeError as e:
+        extras["prefill"] = bench.extra_error(e)
+    line = bench.compact_json(bench.compose_line(_fake_measurements(), extras, _fake_cpu()))
+    assert len(line.encode()) <= 1500
+    assert json.loads(line)["prefill"]["error"].startswith("RuntimeError: xxx")
+
+
+def test_round_sig_keeps_ints_strings_and_non_finite():
+    got = bench.round_sig({"a": 1.23456789, "b": [7, "s", float("inf")], "c": {"d": 0.0001234567},
+                           "e": 6156.0507, "f": 999.96, "g": -12345.6})
+    assert got == {"a": 1.235, "b": [7, "s", float("inf")], "c": {"d": 0.0001235},
+                   "e": 6156, "f": 1000, "g": -12350}
+    assert isinstance(got["e"], int) and isinstance(bench.round_sig(85.4799), float)
+
+
+def test_parallel_oracle_runs_the_batch_on_several_processes():
+    # the multi-core baseline: every sequence once per pass, over spawned workers that map
+    # the pools from shared memory; the bytes per pass are the batch's algorithmic bytes
+    import workloads
+    batch = workloads.make_batch("par", 42, "bf16", [300, 50, 700, 16, 129], 8, 2, 64, 16, 120)
+    sample = bench.OracleSample(batch)
+    par = bench.ParallelOracle(sample, 2)
+    try:
+        assert sorted(i for t in par.tasks for i in t) == list(range(5))
+        assert par.pass_bytes == bench.read_bytes(batch.lens_list(), 8, 2, 64, 2, 16)
+        walls = [par.one_pass() for _ in range(2)]
+        assert all(w > 0 for w in walls)
+        assert par.cpu_s > 0
+    finally:
+        par.close()

@@ -260,18 +260,20 @@ def test_small_chunks_on_the_decode_kernel(lib, dtype, hq, hkv, d, bs, n_q, lens
     assert_attn_close(out, _ref(base, q), base.dtype)
 
 
-def test_warp_specialized_wait_time_out_is_reported(lib, monkeypatch):
+def test_warp_specialized_wait_time_out_is_reported(lib):
     # the load warps announce no key tile (test hook), so the MMA and softmax waits run
     # out; the call reports PA_DEV_TIMEOUT, zeroes its outputs and leaves the context usable
     base = workloads.make_batch("wstimeout", 50, "bf16", [300], 4, 1, 64, 16, 30)
     q = _chunk_batch(base, 64)                  # 64 queries x 4 heads = 256 rows: one CTA
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
-    monkeypatch.setenv("PA_TEST_WITHHOLD_TILES", "1")
-    out = _run(lib, base, q, err)
-    torch.cuda.synchronize()
+    lib.pa_test_set_withhold_tiles(True)
+    try:
+        out = _run(lib, base, q, err)
+        torch.cuda.synchronize()
+    finally:
+        lib.pa_test_set_withhold_tiles(False)
     assert int(err.item()) == lib.PA_DEV_TIMEOUT
     assert torch.all(out == 0)
-    monkeypatch.delenv("PA_TEST_WITHHOLD_TILES")
     err.zero_()
     out = _run(lib, base, q, err)               # the same call runs normally afterwards
     torch.cuda.synchronize()
