@@ -166,9 +166,10 @@ def test_tensor_core_bad_page_is_reported_and_zeroed(lib):
     assert_attn_close(out[:2], _ref(base, q, [0, 1]), base.dtype)
 
 
-def test_prefill_4096_sampled_rows(lib):
-    # the measured prefill launch (8 prompts x 4096 tokens, head_dim 128), checked on
-    # sampled queries of two prompts against attention over their causal prefixes
+def test_prefill_4096_whole_prompt_and_sampled_rows(lib):
+    # the measured prefill launch (8 prompts x 4096 tokens, head_dim 128): one whole prompt
+    # (every query and head) against the oracle's chunked read, and sampled queries of two
+    # more prompts against attention over their causal prefixes
     base = workloads.make_batch("prefill_d128", 6, "bf16", [4096] * 8, 32, 8, 128, 16, 8 * 256,
                                 device=DEV)
     gen = torch.Generator(device=DEV)
@@ -187,6 +188,20 @@ def test_prefill_4096_sampled_rows(lib):
                 ref, _ = oracle.attend(host_f32(q[b, i, h]), k[:i + 1, h // 4], v[:i + 1, h // 4],
                                        base.scale)
                 assert_attn_close(out[b, i, h], ref, base.dtype, f"b{b} i{i} h{h}")
+    # prompt 3 whole: the oracle's chunked read, one kv head (and its 4 query heads) at a
+    # time on float64 copies of the prompt's pages (heads are independent in the definition)
+    b = 3
+    pages = base.block_table[b].long()
+    kp = base.k_pool.index_select(0, pages).double().cpu().numpy()     # [256, 16, 8, 128]
+    vp = base.v_pool.index_select(0, pages).double().cpu().numpy()
+    qb = q[b:b + 1].double().cpu().numpy()                              # [1, 4096, 32, 128]
+    got = out[b:b + 1]
+    for g in range(8):
+        ref = oracle.paged_decode_chunk(np.ascontiguousarray(qb[:, :, 4 * g:4 * g + 4]),
+                                        np.ascontiguousarray(kp[:, :, g:g + 1]),
+                                        np.ascontiguousarray(vp[:, :, g:g + 1]),
+                                        np.arange(256)[None, :], np.array([4096]), base.scale, 16)
+        assert_attn_close(got[:, :, 4 * g:4 * g + 4], ref, base.dtype, f"prompt 3 kv head {g}")
 
 
 # ------------------------------- warp-specialized tcgen05 path (>= 256 rows per kv head)

@@ -68,7 +68,11 @@ def test_ragged8b_full_size_sampled(lib):
     assert int(err.item()) == 0
     assert int(items[:, 0].unique().numel()) == g.num_seqs
     lens = g.lens_list()
-    for b in sorted({0, 255, int(np.argmax(lens)), int(np.argmin(lens))}):
+    # the 4 longest, the 4 shortest and every 10th sequence: 34 of 256
+    order = np.argsort(lens)
+    picks = sorted({int(x) for x in order[:4]} | {int(x) for x in order[-4:]} |
+                   set(range(0, 256, 10)))
+    for b in picks:
         assert_attn_close(out[b], oracle_seq(g, b), g.dtype, f"seq {b}")
     del g, out
     torch.cuda.empty_cache()
