@@ -17,21 +17,22 @@
 //                announced once the warp's own copies have landed
 //   warps 1, 2   MMA: lane 0 of warp 1 + k issues S_k = Q_k . K^T and
 //                O_k += P_k . V for Q tile k (tcgen05.mma, fp32 accumulators
-//                in tensor memory) and commits each to an mbarrier; QK(j + 2)
+//                in tensor memory) and commits each to an mbarrier; QK(j + NB)
 //                goes right after P.V(j), into the S buffer P.V(j) has read
+//                (NB = 3 S buffers per Q tile at head_dim 64, 2 at 128)
 //   warps 4-7    softmax of Q tile 0, warps 8-11 of Q tile 1: thread r of a
 //                group owns row r (tensor-memory lane r), reads its S row,
 //                writes its P row back over S as 16-bit pairs, and moves
 //                the reference max (rescaling its O row) only when a score
 //                passes it by more than 2^8
 //
-// While the softmax warps of one Q tile work on key tile j, S(j + 1) is
-// already in tensor memory, the tensor core runs the other products, and
+// While the softmax warps of one Q tile work on key tile j, S(j + 1) (and at
+// head_dim 64 S(j + 2)) is already in tensor memory, the tensor core runs the other products, and
 // the load warps fetch the next tiles.  Two Q tiles share every K/V tile, so
 // each copy feeds twice the math.
 //
-// Tensor memory: S_0[0..1] | S_1[0..1] (64 columns each) | O_0 | O_1
-// (head_dim each).  mbarriers: full/empty per ring stage, and per Q tile and
+// Tensor memory: S_0[0..NB-1] | S_1[0..NB-1] (64 columns each) | O_0 | O_1
+// (head_dim each): 512 columns at head_dim 64 (NB 3) and at 128 (NB 2).  mbarriers: full/empty per ring stage, and per Q tile and
 // S buffer s (S ready), p (P written, one arrival per softmax warp), o (P.V
 // done: the buffer and O free again); at head_dim 128 also one per softmax
 // group for taking turns at the exponentials.  One barrier per buffer means
@@ -58,7 +59,6 @@ constexpr int kQRows = 128;                  // rows of one Q tile (the MMA M)
 constexpr int kQTiles = 2;                   // Q tiles per CTA
 constexpr int kCtaRows = kQRows * kQTiles;
 constexpr int kKeyTile = 64;                 // tokens per K/V tile
-constexpr int kStages = 4;                   // K/V ring depth
 constexpr int kThreads = 384;                // 12 warps
 constexpr int kAllocWarp = 2, kSoftmaxWarp0 = 4;
 constexpr int kLoaders = 2;                  // warps 0 and 3 load tiles j = 0, 1 (mod 2)
@@ -66,13 +66,34 @@ constexpr int kLoaders = 2;                  // warps 0 and 3 load tiles j = 0, 
 // issue takes ~100+ cycles, so two issuers keep the tensor pipe about twice as busy
 constexpr float kRescaleLog2 = 8.f;
 
+// S buffers per Q tile and K/V ring stages at head_dim 64 (see WsShape)
+#ifndef PA_WS_SBUF_D64
+#define PA_WS_SBUF_D64 3
+#endif
+#ifndef PA_WS_STAGES_D64
+#define PA_WS_STAGES_D64 6
+#endif
+
 template <int D>
 struct WsShape {
   static constexpr int kQBytes = kQRows * D * 2;     // one Q tile: [kb][128 rows][128 B]
   static constexpr int kKVBytes = kKeyTile * D * 2;  // one K or V tile: [kb][64 rows][128 B]
+  // K/V ring depth: QK(j + kSBuf) needs key tile j + kSBuf, whose stage was released by
+  // P.V(j + kSBuf - kStages); the stages beyond kSBuf are the loads' time to arrive.
+  // 6 stages at head_dim 64 (16 KB each, 129 KB with Q), 4 at 128 (32 KB each, 193 KB).
+  // Same-GPU A/B at head_dim 64 (S buffers x stages, prefill 8 x 4096 / 64-query chunks
+  // at history 4096, us): 2 x 4 848 / 231, 2 x 8 856 / 224, 3 x 8 852 / 223,
+  // 3 x 6 846 / 223; 3 buffers with 4 stages took 922 / 301 (the key loads then sit on
+  // the critical path).
+  static constexpr int kStages = D <= 64 ? PA_WS_STAGES_D64 : 4;
   static constexpr int kSmem = kQTiles * kQBytes + kStages * 2 * kKVBytes + 1024;
-  // S_k in two buffers (tiles j even / odd) per Q tile, then O_k
-  static constexpr int kSCols = kQTiles * 2 * kKeyTile;
+  // S_k in kSBuf buffers per Q tile (tile j in buffer j % kSBuf), then O_k.  Three
+  // buffers at head_dim 64 (3 * 2 * 64 + 2 * 64 = 512 columns, all of tensor memory),
+  // two at 128: QK(j + kSBuf) can only overwrite the buffer P.V(j) has finished
+  // reading, so the chain softmax(j) -> P.V(j) -> QK(j + kSBuf) -> softmax(j + kSBuf)
+  // spreads over kSBuf tiles.
+  static constexpr int kSBuf = D <= 64 ? PA_WS_SBUF_D64 : 2;
+  static constexpr int kSCols = kQTiles * kSBuf * kKeyTile;
   static constexpr int kTmemUsed = kSCols + kQTiles * D;
   static constexpr int kTmemCols = kTmemUsed <= 256 ? 256 : 512;
 };
@@ -110,8 +131,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const int withhold) {
   using S = WsShape<D>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
+  constexpr int NB = S::kSBuf;
+  constexpr int kStages = S::kStages;
   __shared__ uint64_t bar_full[kStages], bar_empty[kStages];
-  __shared__ uint64_t bar_s[kQTiles][2], bar_p[kQTiles][2], bar_o[kQTiles][2];
+  __shared__ uint64_t bar_s[kQTiles][NB], bar_p[kQTiles][NB], bar_o[kQTiles][NB];
   __shared__ uint64_t bar_turn[kQTiles];  // softmax groups take turns at the exponentials
   __shared__ uint32_t tmem_base;
   __shared__ int s_bad, s_fail;
@@ -141,12 +164,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 #pragma unroll
     for (int k = 0; k < kQTiles; ++k) {
-      mbar_init(&bar_s[k][0], 1);
-      mbar_init(&bar_s[k][1], 1);
-      mbar_init(&bar_p[k][0], kQRows / 32);  // one arrival per softmax warp
-      mbar_init(&bar_p[k][1], kQRows / 32);
-      mbar_init(&bar_o[k][0], 1);
-      mbar_init(&bar_o[k][1], 1);
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        mbar_init(&bar_s[k][nb], 1);
+        mbar_init(&bar_p[k][nb], kQRows / 32);  // one arrival per softmax warp
+        mbar_init(&bar_o[k][nb], 1);
+      }
       mbar_init(&bar_turn[k], kQRows / 32);
     }
   }
@@ -224,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool warp_live = is_softmax && base0 + k_sm * kQRows + quad * 32 < rows_total;
   const int my_nt = is_softmax ? (k_sm == 0 ? nt[0] : nt[1]) : 0;
   const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
-  const uint32_t t_s0 = tmem + k_sm * 2 * kKeyTile + t_lane;  // S buffer 0; buffer 1 at +64
+  const uint32_t t_s0 = tmem + k_sm * NB * kKeyTile + t_lane;  // S buffer 0; buffer b at +64 b
   const uint32_t t_o = tmem + S::kSCols + k_sm * D + t_lane;
   const float sl2 = fmaxf(fabsf(p.scale_log2), 1e-30f);
   float m_ref = -CUDART_INF_F;  // reference max (raw units) of the exponent
@@ -338,8 +361,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     cp_async_wait_all();
   } else if (mma_k >= 0) {
     // ---------------------------------------------------------- MMA warps
-    // Warp 1 + k issues Q tile k's products: QK(0) and QK(1), then for each
-    // tile j: P.V(j), release of stage j, and QK(j + 2) into the S buffer
+    // Warp 1 + k issues Q tile k's products: QK(0) .. QK(NB - 1), then for each
+    // tile j: P.V(j), release of stage j, and QK(j + NB) into the S buffer
     // P.V(j) has just read.  So S(j + 1) is ready while the softmax works on
     // tile j, and the softmax warps do not wait for the tensor core.
     if (lane == 0) {
@@ -348,47 +371,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t id_pv = idesc<T>(kQRows, D, true, false);
       const uint32_t qs_u = smem_u32(sq + k * S::kQBytes);
       const uint32_t t_o_k = tmem + S::kSCols + k * D;
-      // S_k[j & 1] = Q_k . K_j^T, once tile j is in and the buffer is free (P_k
-      // of tile j - 2 has gone through P.V: completion (j - 2) / 2 of its
+      // S_k[j % NB] = Q_k . K_j^T, once tile j is in and the buffer is free (P_k
+      // of tile j - NB has gone through P.V: completion (j - NB) / NB of its
       // barrier, the last one it can have had, since P.V(j) needs this S)
       auto issue_qk = [&](int j) -> bool {
         if (!wait_phase(smem_u32(&bar_full[j % kStages]), (j / kStages) & 1)) return false;
-        if (j >= 2 && !wait_phase(smem_u32(&bar_o[k][j & 1]), ((j >> 1) - 1) & 1)) return false;
+        if (j >= NB && !wait_phase(smem_u32(&bar_o[k][j % NB]), ((j / NB) - 1) & 1)) return false;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t ks_u = smem_u32(skv + (2 * (j % kStages)) * S::kKVBytes);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t kb = ks >> 2, kin = (ks & 3) * 32;
-          mma_f16(tmem + (2 * k + (j & 1)) * kKeyTile,
+          mma_f16(tmem + (NB * k + (j % NB)) * kKeyTile,
                   sw128_desc(qs_u + kb * (kQRows * 128) + kin, 16, 1024),
                   sw128_desc(ks_u + kb * (kKeyTile * 128) + kin, 16, 1024), id_qk, ks > 0);
         }
-        commit(smem_u32(&bar_s[k][j & 1]));
+        commit(smem_u32(&bar_s[k][j % NB]));
         return true;
       };
       // O_k += P_k . V_j once the softmax warps of Q tile k have written P_k
       auto issue_pv = [&](int j) -> bool {
-        if (!wait_phase(smem_u32(&bar_p[k][j & 1]), (j >> 1) & 1)) return false;
+        if (!wait_phase(smem_u32(&bar_p[k][j % NB]), (j / NB) & 1)) return false;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t vs_u = smem_u32(skv + (2 * (j % kStages) + 1) * S::kKVBytes);
-        const uint32_t t_s = tmem + (2 * k + (j & 1)) * kKeyTile;
+        const uint32_t t_s = tmem + (NB * k + (j % NB)) * kKeyTile;
 #pragma unroll
         for (int kk = 0; kk < kKeyTile / 16; ++kk)
           mma_f16_ta(t_o_k, t_s + kk * 8, sw128_desc(vs_u + kk * 2048, kKeyTile * 128, 1024),
                      id_pv, (j > 0 || kk > 0));
-        commit(smem_u32(&bar_o[k][j & 1]));
+        commit(smem_u32(&bar_o[k][j % NB]));
         return true;
       };
       const int my = k == 0 ? nt[0] : nt[1];
-      if (my > 0 && !issue_qk(0)) fail = true;
-      if (!fail && my > 1 && !issue_qk(1)) fail = true;
+      for (int j = 0; j < NB && j < my && !fail; ++j)
+        if (!issue_qk(j)) fail = true;
       for (int j = 0; j < my && !fail; ++j) {
         if (!issue_pv(j)) {
           fail = true;
           break;
         }
         commit(smem_u32(&bar_empty[j % kStages]));  // stage j is free once P.V(j) is done
-        if (j + 2 < my && !issue_qk(j + 2)) fail = true;
+        if (j + NB < my && !issue_qk(j + NB)) fail = true;
       }
       // tiles this Q tile does not need: release each after it arrived, so that
       // a stage is never released ahead of its fill
@@ -419,12 +442,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // own progress, so a parity wait never sees two completions.
     const int n_pair = (nt[0] > 0 && nt[1] > 0) ? min(nt[0], nt[1]) : 0;
     for (int j = 0; j < my_nt; ++j) {
-      if (!wait_phase(smem_u32(&bar_s[k][j & 1]), (j >> 1) & 1)) {
+      if (!wait_phase(smem_u32(&bar_s[k][j % NB]), (j / NB) & 1)) {
         fail = true;
         break;
       }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const uint32_t t_s = t_s0 + (j & 1) * kKeyTile;
+      const uint32_t t_s = t_s0 + (j % NB) * kKeyTile;
       const int tok0 = t_lo + j * kKeyTile;
       float s[kKeyTile];
       // S row of this thread, -inf past its last key
@@ -487,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // rescale this warp's O rows once the previous P.V has finished with them
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          if (!wait_phase(smem_u32(&bar_o[k][(j - 1) & 1]), ((j - 1) >> 1) & 1)) fail = true;
+          if (!wait_phase(smem_u32(&bar_o[k][(j - 1) % NB]), ((j - 1) / NB) & 1)) fail = true;
           asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
           if (!__any_sync(0xffffffffu, fail)) {
 #pragma unroll
@@ -503,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       __syncwarp();  // the warp's P (and O) stores are done
-      if (lane == 0) mbar_arrive(&bar_p[k][j & 1]);
+      if (lane == 0) mbar_arrive(&bar_p[k][j % NB]);
       if (__any_sync(0xffffffffu, fail)) {
         fail = true;
         break;
@@ -511,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // the last P.V of this Q tile
     if (my_nt > 0 && !fail &&
-        !wait_phase(smem_u32(&bar_o[k][(my_nt - 1) & 1]), ((my_nt - 1) >> 1) & 1))
+        !wait_phase(smem_u32(&bar_o[k][(my_nt - 1) % NB]), ((my_nt - 1) / NB) & 1))
       fail = true;
   }
 
