@@ -95,9 +95,11 @@ pa::DecodeParams make_params(const void *q, const void *k_pool, const void *v_po
 
 pa_status launched(cudaError_t err) { return err == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
 
-// f16/bf16 rows the tensor-core kernel covers go there; the rest to the CUDA cores.
+// f16/bf16 rows the tensor-core kernel covers go there, fp32 to its CUDA-core
+// read, the rest (f16/bf16 at other head dims) to the general CUDA-core read.
 cudaError_t launch_read(const pa::DecodeParams &p, pa_dtype dtype, cudaStream_t stream) {
   if (pa::mma_supports(dtype, p.head_dim, p.group)) return pa::launch_decode_mma(p, dtype, stream);
+  if (dtype == PA_F32 && p.chunk_len == 1) return pa::launch_decode_f32(p, stream);
   return pa::launch_decode_simt(p, dtype, stream);
 }
 

@@ -112,6 +112,8 @@ struct MergeParams {
 
 // CUDA-core read: every dtype, query groups of up to 8 heads.
 cudaError_t launch_decode_simt(const DecodeParams &p, pa_dtype dtype, cudaStream_t stream);
+// CUDA-core read for fp32 caches (pa_decode_f32.cu): groups of up to 8.
+cudaError_t launch_decode_f32(const DecodeParams &p, cudaStream_t stream);
 // Tensor-core read: f16/bf16, head_dim in {32, 48, 64, 96, 128, 256}, groups of up to 16.
 bool mma_supports(pa_dtype dtype, int head_dim, int group);
 // The chunked read of up to 16 (query, head) columns per kv head at head_dim

@@ -231,6 +231,43 @@ def test_decode_other_shapes(lib, dtype, hq, hkv, d, bs):
     assert_attn_close(merged, ref, cpu.dtype, "split+merge")
 
 
+@pytest.mark.parametrize("hq,hkv,d", [(32, 8, 64), (16, 2, 128), (8, 8, 256), (12, 4, 36)])
+def test_f32_cache_at_batch_size(lib, hq, hkv, d):
+    # the fp32 read (CUDA cores) on 64 ragged sequences up to 1100 tokens, every sequence
+    # against the oracle, single pass and split into 7-page runs + merge
+    gen = torch.Generator().manual_seed(d)
+    lens = [1, 15, 16, 17] + torch.randint(1, 1101, (60,), generator=gen).tolist()
+    pages = sum(-(-n // 16) for n in lens) + 9
+    cpu = workloads.make_batch("f32_batch", 23, "f32", lens, hq, hkv, d, 16, pages)
+    gpu = cpu.to(DEV)
+    err = _err_buf()
+    _append(lib, gpu, err)
+    out = _decode(lib, gpu, err)
+    _, _, merged = _split(lib, gpu, 7, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    k2, v2 = _host_after_append(cpu)
+    ref = oracle.paged_decode(host_f32(cpu.q), k2, v2, cpu.block_table.numpy(),
+                              cpu.seq_lens.numpy(), cpu.scale, 16)
+    assert_attn_close(out, ref, cpu.dtype, "single pass")
+    assert_attn_close(merged, ref, cpu.dtype, "split + merge")
+
+
+def test_f32_bad_page_is_reported_and_zeroed(lib):
+    cpu = workloads.make_batch("f32_bad", 24, "f32", [40, 300, 129], 8, 2, 64, 16, 40)
+    cpu.block_table[1, 7] = cpu.num_pages + 3
+    gpu = cpu.to(DEV)
+    err = _err_buf()
+    out = _decode(lib, gpu, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 1
+    assert torch.all(out[1] == 0)
+    ref = oracle.paged_decode(host_f32(cpu.q[[0, 2]]), host_f32(cpu.k_pool), host_f32(cpu.v_pool),
+                              cpu.block_table[[0, 2]].numpy(), cpu.seq_lens[[0, 2]].numpy(),
+                              cpu.scale, 16)
+    assert_attn_close(out[[0, 2]], ref, cpu.dtype)
+
+
 # ---------------------------------------------------------------- split-KV + merge
 
 
