@@ -38,10 +38,14 @@ constexpr float kLazyLog2 = 8.f;  // the reference moves when a score passes it 
 // Shape per head-dim bucket: NP channel pairs per lane (head_dim <= 64 NP), warps
 // per CTA and ring stages per warp.  Shared memory per CTA (group 8): 105 KB at
 // head_dim 64 (two CTAs per SM), 139 KB at 128, 141 KB at 256.
+#ifndef PA_F32_STAGES_D64  // ring stages per warp at head_dim <= 64
+#define PA_F32_STAGES_D64 3
+#endif
+
 template <int NP>
 struct F32Shape {
   static constexpr int kWarps = NP <= 2 ? 4 : 2;
-  static constexpr int kStages = NP == 1 ? 3 : 2;
+  static constexpr int kStages = NP == 1 ? PA_F32_STAGES_D64 : 2;
 };
 
 template <int NP>
@@ -54,8 +58,10 @@ size_t f32_smem(int d, int group_max) {
   return (q + probs + (ring > combine ? ring : combine)) * sizeof(float);
 }
 
-// GMAX: group size bound (1, 2, 4, 8); NP: channel pairs per lane.
-template <int GMAX, int NP>
+// GMAX: group size bound (1, 2, 4, 8); NP: channel pairs per lane; DT: the head dim
+// when it is fixed at compile time (32, 64, 128, 256: index math by shifts, loops
+// unrolled), else 0 (read from the parameters).
+template <int GMAX, int NP, int DT>
 __global__ void __launch_bounds__(kMaxThreads) decode_f32_kernel(const DecodeParams p) {
   constexpr int stages = F32Shape<NP>::kStages;
   extern __shared__ __align__(16) float sm[];
@@ -64,7 +70,7 @@ __global__ void __launch_bounds__(kMaxThreads) decode_f32_kernel(const DecodePar
   const int nwarps = blockDim.x >> 5;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int tok = lane & (kTok - 1), half = lane >> 4;
-  const int D = p.head_dim, PK = D + 4, nch = D >> 2;
+  const int D = DT > 0 ? DT : p.head_dim, PK = D + 4, nch = D >> 2;
   const int G = p.group;
   const int hkv = p.num_kv_heads;
   const int g = blockIdx.x % hkv;
@@ -199,13 +205,19 @@ __global__ void __launch_bounds__(kMaxThreads) decode_f32_kernel(const DecodePar
 #pragma unroll
     for (int h = 0; h < GMAX; ++h) s[h] = 0.f;
     const float *krow = ks + tok * PK;
-    for (int c = c0; c < c1; ++c) {
+    auto dot_chunk = [&](int c) {
       const float4 k4 = *reinterpret_cast<const float4 *>(krow + c * 4);
 #pragma unroll
       for (int h = 0; h < GMAX; ++h) {
         const float4 q4 = *reinterpret_cast<const float4 *>(q_s + h * D + c * 4);
         s[h] = fmaf(q4.x, k4.x, fmaf(q4.y, k4.y, fmaf(q4.z, k4.z, fmaf(q4.w, k4.w, s[h]))));
       }
+    };
+    if constexpr (DT > 0) {  // the two halves are DT / 8 chunks each
+#pragma unroll
+      for (int k = 0; k < DT / 8; ++k) dot_chunk(half * (DT / 8) + k);
+    } else {
+      for (int c = c0; c < c1; ++c) dot_chunk(c);
     }
     const bool valid = tok0 + tok < t_end;
 #pragma unroll
@@ -241,8 +253,19 @@ __global__ void __launch_bounds__(kMaxThreads) decode_f32_kernel(const DecodePar
 #pragma unroll 8
     for (int t = 0; t < kTok; ++t) {
       float pt[GMAX];
+      if constexpr (GMAX >= 4) {
 #pragma unroll
-      for (int h = 0; h < GMAX; ++h) pt[h] = my_p[t * GMAX + h];
+        for (int h = 0; h < GMAX; h += 4) {
+          const float4 v4 = *reinterpret_cast<const float4 *>(my_p + t * GMAX + h);
+          pt[h] = v4.x;
+          pt[h + 1] = v4.y;
+          pt[h + 2] = v4.z;
+          pt[h + 3] = v4.w;
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) pt[h] = my_p[t * GMAX + h];
+      }
 #pragma unroll
       for (int i2 = 0; i2 < NP; ++i2) {
         const int pair = lane + 32 * i2;
@@ -315,10 +338,10 @@ __global__ void __launch_bounds__(kMaxThreads) decode_f32_kernel(const DecodePar
   }
 }
 
-template <int GMAX, int NP>
+template <int GMAX, int NP, int DT>
 cudaError_t launch_np(const DecodeParams &p, cudaStream_t stream) {
   const int smem = static_cast<int>(f32_smem<NP>(p.head_dim, GMAX));
-  auto kern = decode_f32_kernel<GMAX, NP>;
+  auto kern = decode_f32_kernel<GMAX, NP, DT>;
   cudaError_t err = set_max_smem(reinterpret_cast<const void *>(kern), smem);
   if (err != cudaSuccess) return err;
   dim3 grid(p.num_splits * p.num_kv_heads, p.num_seqs);
@@ -327,9 +350,15 @@ cudaError_t launch_np(const DecodeParams &p, cudaStream_t stream) {
 
 template <int GMAX>
 cudaError_t launch_g(const DecodeParams &p, cudaStream_t stream) {
-  if (p.head_dim <= 64) return launch_np<GMAX, 1>(p, stream);
-  if (p.head_dim <= 128) return launch_np<GMAX, 2>(p, stream);
-  return launch_np<GMAX, 4>(p, stream);
+  switch (p.head_dim) {
+    case 32: return launch_np<GMAX, 1, 32>(p, stream);
+    case 64: return launch_np<GMAX, 1, 64>(p, stream);
+    case 128: return launch_np<GMAX, 2, 128>(p, stream);
+    case 256: return launch_np<GMAX, 4, 256>(p, stream);
+  }
+  if (p.head_dim <= 64) return launch_np<GMAX, 1, 0>(p, stream);
+  if (p.head_dim <= 128) return launch_np<GMAX, 2, 0>(p, stream);
+  return launch_np<GMAX, 4, 0>(p, stream);
 }
 
 }  // namespace
