@@ -63,7 +63,7 @@ def parse_args():
     ap.add_argument("--no-extras", action="store_true",
                     help="headline step only (no sweep, long-context, ragged, CPU baseline)")
     ap.add_argument("--only", choices=["sweep", "longctx", "ragged8b", "dense_vs_sdpa", "chunk",
-                                       "prefill"],
+                                       "prefill", "f32", "floor"],
                     help="run one extra section alone and print its JSON (for profiling)")
     return ap.parse_args()
 
@@ -457,7 +457,9 @@ def main():
                "ragged8b": lambda: ragged(pa, workloads, torch, dev, peak),
                "dense_vs_sdpa": lambda: dense_vs_sdpa(pa, workloads, torch, dev, peak),
                "chunk": lambda: chunk(pa, workloads, torch, dev, peak),
-               "prefill": lambda: prefill(pa, workloads, torch, dev)}
+               "prefill": lambda: prefill(pa, workloads, torch, dev),
+               "f32": lambda: f32_read(pa, workloads, torch, dev, peak),
+               "floor": lambda: launch_floor(pa, workloads, torch, dev, peak)}
         print(json.dumps({args.only: fns[args.only]()[1]}), flush=True)
         return
     dist = None
@@ -927,6 +929,50 @@ def chunk_longctx(pa, workloads, torch, dev, peak, flush):
     del g
     torch.cuda.empty_cache()
     return rows
+
+
+def launch_floor(pa, workloads, torch, dev, peak):
+    """The read's fixed cost per launch at history 1024 (B 64): the same batch with every
+    length 0 (the same 512-CTA grid, reading only q and the lengths) beside the real read,
+    and two events with nothing between them, each after an L2 flush.  Launch order (for an
+    ncu capture of decode_mma): 3 + 30 empty reads, then 3 + 30 real ones."""
+    flush = L2Flush(torch, dev)
+    g = workloads.llama1b(1024, device=str(dev))
+    out = torch.empty_like(g.q)
+    zero = torch.zeros_like(g.seq_lens)
+    empty = lambda: pa.pa_decode(out, g.q, g.k_pool, g.v_pool, g.block_table, zero, g.scale)
+    real = lambda: pa.pa_decode(out, g.q, g.k_pool, g.v_pool, g.block_table, g.seq_lens, g.scale)
+    e_med, e_min = _time_launches(empty, torch, flush)
+    r_med, r_min = _time_launches(real, torch, flush)
+    n_med, n_min = _time_launches(lambda: None, torch, flush)
+    rb = read_bytes(g.lens_list(), 32, 8, 64, 2, 16)
+    detail = {"us_events_alone": 1e3 * n_med, "us_empty_read": 1e3 * e_med,
+              "us_read_h1024": 1e3 * r_med, "us_read_h1024_min": 1e3 * r_min,
+              "frac_read_h1024": rb / (r_med * 1e-3) / 1e9 / peak}
+    del g, out
+    torch.cuda.empty_cache()
+    return {k: detail[k] for k in ("us_empty_read", "us_read_h1024")}, detail
+
+
+def f32_read(pa, workloads, torch, dev, peak):
+    """The fp32 read (CUDA cores) on llama1b-shaped batches (B 64, Hq 32 / Hkv 8) at
+    head_dim 64 and 128, histories 1024 and 4096, L2 flushed before each launch."""
+    flush = L2Flush(torch, dev)
+    rows = []
+    for d in (64, 128):
+        for h in (1024, 4096):
+            g = workloads.make_batch(f"f32_d{d}_h{h}", 2, "f32", [h] * 64, 32, 8, d, 16,
+                                     64 * (h // 16) + 16, device=str(dev))
+            out = torch.empty_like(g.q)
+            fn = lambda: pa.pa_decode(out, g.q, g.k_pool, g.v_pool, g.block_table, g.seq_lens,
+                                      g.scale)
+            med, mn = _time_launches(fn, torch, flush, iters=20)
+            rb = read_bytes(g.lens_list(), 32, 8, d, 4, 16)
+            rows.append({"head_dim": d, "history": h, "us_median": 1e3 * med, "us_min": 1e3 * mn,
+                         "gbs": rb / (med * 1e-3) / 1e9, "frac": rb / (med * 1e-3) / 1e9 / peak})
+            del g, out
+            torch.cuda.empty_cache()
+    return {f"d{r['head_dim']}_h{r['history']}": r["frac"] for r in rows}, rows
 
 
 def measured_bf16_tflops():

@@ -1,4 +1,6 @@
-// Paged decode attention on the CUDA cores (fp32 FMA), any supported dtype.
+// Paged decode attention on the CUDA cores (fp32 FMA) for f16/bf16 caches at
+// head dims the tensor-core read does not cover (fp32 caches have their own
+// read, pa_decode_f32.cu).
 //
 // One CTA per (sequence, kv head, split).  The CTA walks its token range of
 // the block table ("Three Attention Kernels", section "3. Paged KV-cache
@@ -325,21 +327,17 @@ cudaError_t launch_group(const DecodeParams &p, int nch, int tg_log2, cudaStream
 
 template <typename T>
 cudaError_t launch_typed(const DecodeParams &p, cudaStream_t stream) {
-  const int nch = p.head_dim * static_cast<int>(sizeof(T)) / 16;
-  const int cpl = nch > 32 ? 2 : 1;
-  const int tg_log2 = ceil_log2((nch + cpl - 1) / cpl);
-  if (cpl == 1) return launch_group<T, 1>(p, nch, tg_log2, stream);
-  if constexpr (sizeof(T) == 4) return launch_group<T, 2>(p, nch, tg_log2, stream);
-  return cudaErrorInvalidValue;  // 16-bit rows never need more than 32 chunks
+  const int nch = p.head_dim * static_cast<int>(sizeof(T)) / 16;  // <= 32 at head_dim <= 256
+  return launch_group<T, 1>(p, nch, ceil_log2(nch), stream);
 }
 
 }  // namespace
 
 cudaError_t launch_decode_simt(const DecodeParams &p, pa_dtype dtype, cudaStream_t stream) {
   switch (dtype) {
-    case PA_F32: return launch_typed<float>(p, stream);
     case PA_F16: return launch_typed<__half>(p, stream);
     case PA_BF16: return launch_typed<__nv_bfloat16>(p, stream);
+    case PA_F32: break;  // fp32 caches: launch_decode_f32
   }
   return cudaErrorInvalidValue;
 }

@@ -110,7 +110,7 @@ struct MergeParams {
   int32_t num_splits, head_dim;
 };
 
-// CUDA-core read: every dtype, query groups of up to 8 heads.
+// CUDA-core read for f16/bf16 at head dims outside the tensor-core list, groups of up to 8.
 cudaError_t launch_decode_simt(const DecodeParams &p, pa_dtype dtype, cudaStream_t stream);
 // CUDA-core read for fp32 caches (pa_decode_f32.cu): groups of up to 8.
 cudaError_t launch_decode_f32(const DecodeParams &p, cudaStream_t stream);
