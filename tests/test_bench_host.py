@@ -250,3 +250,17 @@ def test_parallel_oracle_runs_the_batch_on_several_processes():
         assert par.cpu_s > 0
     finally:
         par.close()
+
+
+def test_cpu_baseline_falls_back_to_one_thread_without_shared_memory(monkeypatch):
+    # a host whose shared memory cannot hold the pools still reports the single-core figure
+    import workloads
+
+    class NoShm:
+        def __init__(self, *a, **k):
+            raise OSError("no space left on device")
+
+    monkeypatch.setattr(bench, "ParallelOracle", NoShm)
+    batch = workloads.make_batch("fallback", 43, "bf16", [64, 32], 8, 2, 64, 16, 12)
+    got = bench.cpu_baseline(batch, 64, single_budget_s=0.2, multi_budget_s=0.2)
+    assert got["cores"] == 1 and got["value"] > 0 and "OSError" in got["sample"]
