@@ -145,16 +145,30 @@ __global__ void __launch_bounds__(kThreads, TcShape<D>::kMinBlocks)
   const int32_t *bt_row = p.block_table + static_cast<size_t>(b) * p.max_blocks;
   const T *kpool = static_cast<const T *>(p.k_pool);
   const T *vpool = static_cast<const T *>(p.v_pool);
-  auto load_tile = [&](int j, int stage) {
+  // Thread tid copies chunk tid % (D / 8) of rows tid / (D / 8) + k * kRowStep of a tile.
+  // Their page ids are read one tile ahead of the copies, so no copy waits for a
+  // block-table load.
+  constexpr int kCopies = kKeyTile * (D / 8) / kThreads;  // rows per thread: 4, or 8 at 128
+  constexpr int kRowStep = kThreads / (D / 8);
+  const int c_own = tid % (D / 8), tr0 = tid / (D / 8);
+  auto fetch_pages = [&](int j, int (&pid)[kCopies]) {
+#pragma unroll
+    for (int k = 0; k < kCopies; ++k) {
+      const int t = t_lo + j * kKeyTile + tr0 + k * kRowStep;
+      pid[k] = (j < ntiles && t < kv_end) ? __ldg(bt_row + (t >> bs_log2)) : -1;
+    }
+  };
+  auto load_tile = [&](int j, int stage, const int (&pid)[kCopies]) {
     unsigned char *ks = skv + (2 * stage) * S::kKVBytes;
     unsigned char *vs = ks + S::kKVBytes;
-    for (int idx = tid; idx < kKeyTile * (D / 8); idx += kThreads) {
-      const int tr = idx / (D / 8), c = idx - tr * (D / 8);
+#pragma unroll
+    for (int k = 0; k < kCopies; ++k) {
+      const int tr = tr0 + k * kRowStep, c = c_own;
       const int t = t_lo + j * kKeyTile + tr;
       bool valid = t < kv_end;
       const T *ksrc = kpool, *vsrc = vpool;
       if (valid) {
-        const int page = __ldg(bt_row + (t >> bs_log2));
+        const int page = pid[k];
         if (page < 0 || page >= p.num_pages) {
           report_error(p.dev_err, PA_DEV_BAD_PAGE);
           s_bad = 1;
@@ -171,8 +185,11 @@ __global__ void __launch_bounds__(kThreads, TcShape<D>::kMinBlocks)
       cp_async16(vs + o, vsrc, valid);
     }
   };
-  if (ntiles > 0) load_tile(0, 0);
+  int pid[kCopies];
+  fetch_pages(0, pid);
+  if (ntiles > 0) load_tile(0, 0, pid);
   cp_async_commit();
+  fetch_pages(1, pid);
 
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();  // barrier init, tensor-memory address, s_bad
@@ -190,8 +207,9 @@ __global__ void __launch_bounds__(kThreads, TcShape<D>::kMinBlocks)
 
   for (int j = 0; j < ntiles; ++j) {
     const int stage = j & 1;
-    if (j + 1 < ntiles) load_tile(j + 1, stage ^ 1);
+    if (j + 1 < ntiles) load_tile(j + 1, stage ^ 1, pid);
     cp_async_commit();
+    fetch_pages(j + 2, pid);  // in flight while this tile is computed
     cp_async_wait<1>();  // Q and tile j are in shared memory
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor core
     __syncthreads();
