@@ -3,11 +3,12 @@
 //
 // Same contract as the mma.sync chunk read (nanoserve "Day 23: the real
 // triton.jit paged-attention kernel": query i of a chunk sits at position
-// past + i and sees tokens 0 .. past + i), for chunks of 64 to 255 (query,
-// head) rows per kv head at head_dim 64 and 128 to 255 at head_dim 128;
-// longer ones (a prompt's prefill among them) go to the warp-specialized
-// read.  One CTA owns 128 rows of one (sequence, kv head), one row per
-// thread, and walks the causal key range in 64-token tiles:
+// past + i and sees tokens 0 .. past + i), for chunks of 128 to 255 (query,
+// head) rows per kv head at head_dim 128; longer ones (a prompt's prefill
+// among them) go to the warp-specialized read, and at head_dim 64 the
+// pipelined one-tile read takes this range.  One CTA owns 128 rows of one
+// (sequence, kv head), one row per thread, and walks the causal key range in
+// 64-token tiles:
 //
 //   S [128 x 64] = Q [128 x D] . K_tile^T      tcgen05.mma -> tensor memory
 //   softmax      : thread r loads row r of S (tcgen05.ld), masks, takes the
@@ -17,8 +18,7 @@
 //                                             tensor memory; O stays there too
 //
 // P never touches shared memory, which then holds only Q and two K/V stages:
-// 49 KB at head_dim 64, so four CTAs share an SM (their 4 x 128 tensor-memory
-// columns fill it exactly).
+// 97 KB at head_dim 128, two CTAs per SM (256 tensor-memory columns each).
 //
 // The running max used for the exponent is only moved when a row's max
 // grows by more than 2^8 (then O and l are rescaled, warp by warp, through
@@ -304,6 +304,8 @@ __global__ void __launch_bounds__(kThreads, TcShape<D>::kMinBlocks)
   }
   const bool empty = bad || l == 0.f || !have_o;
   const float inv = empty ? 0.f : 1.f / l;
+  // an empty or bad row stores exact zeros (a skipped tile can leave any bits in O)
+  auto scaled = [&](float x) { return empty ? 0.f : x * inv; };
   const size_t prow = orow * p.num_splits + split;  // used in the split read only
   if (partial && row_ok)  // natural-log lse of the row's scores over this split
     p.partial_lse[prow] =
@@ -322,16 +324,16 @@ __global__ void __launch_bounds__(kThreads, TcShape<D>::kMinBlocks)
 #pragma unroll
       for (int e = 0; e < 32; e += 4)
         *reinterpret_cast<float4 *>(dst + e) =
-            make_float4(o[e] * inv, o[e + 1] * inv, o[e + 2] * inv, o[e + 3] * inv);
+            make_float4(scaled(o[e]), scaled(o[e + 1]), scaled(o[e + 2]), scaled(o[e + 3]));
     } else if (row_ok) {
       T *dst = static_cast<T *>(p.out) + orow * D + cb;
 #pragma unroll
       for (int e = 0; e < 32; e += 8) {
         uint4 w;
-        w.x = Pack2<T>::run(o[e] * inv, o[e + 1] * inv);
-        w.y = Pack2<T>::run(o[e + 2] * inv, o[e + 3] * inv);
-        w.z = Pack2<T>::run(o[e + 4] * inv, o[e + 5] * inv);
-        w.w = Pack2<T>::run(o[e + 6] * inv, o[e + 7] * inv);
+        w.x = Pack2<T>::run(scaled(o[e]), scaled(o[e + 1]));
+        w.y = Pack2<T>::run(scaled(o[e + 2]), scaled(o[e + 3]));
+        w.z = Pack2<T>::run(scaled(o[e + 4]), scaled(o[e + 5]));
+        w.w = Pack2<T>::run(scaled(o[e + 6]), scaled(o[e + 7]));
         *reinterpret_cast<uint4 *>(dst + e) = w;
       }
     }
@@ -357,22 +359,19 @@ cudaError_t launch_d(const ChunkParams &p, cudaStream_t stream) {
 
 template <typename T>
 cudaError_t launch_t(const ChunkParams &p, cudaStream_t stream) {
-  switch (p.head_dim) {
-    case 64: return launch_d<T, 64>(p, stream);
-    case 128: return launch_d<T, 128>(p, stream);
-  }
+  if (p.head_dim == 128) return launch_d<T, 128>(p, stream);
   return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-// At head_dim 64 this read measured faster than the mma.sync one from 64
-// rows per (sequence, kv head) on, even with half of the 128-row tile idle;
-// at head_dim 128 only from a full tile on.
+// At head_dim 128 this read measured faster than the mma.sync one from a full
+// 128-row tile per (sequence, kv head) on.  (At head_dim 64 it was faster from
+// 64 rows on, and the pipelined read is faster still: 16-query chunks of the
+// 64 x 4096-token batch took 129.2 us here, 112.3 us there.)
 bool chunk_tc_supports(pa_dtype dtype, int head_dim, int rows) {
   if (dtype != PA_F16 && dtype != PA_BF16) return false;
-  if (head_dim != 64 && head_dim != 128) return false;
-  return rows >= (head_dim == 64 ? kRows / 2 : kRows);
+  return head_dim == 128 && rows >= kRows;
 }
 
 cudaError_t launch_chunk_tc(const ChunkParams &p, pa_dtype dtype, cudaStream_t stream) {

@@ -32,7 +32,8 @@
 // each copy feeds twice the math.
 //
 // Tensor memory: S_0[0..NB-1] | S_1[0..NB-1] (64 columns each) | O_0 | O_1
-// (head_dim each): 512 columns at head_dim 64 (NB 3) and at 128 (NB 2).  mbarriers: full/empty per ring stage, and per Q tile and
+// (head_dim each): 512 columns at head_dim 64 (NB 3) and at 128 (NB 2).
+// mbarriers: full/empty per ring stage, and per Q tile and
 // S buffer s (S ready), p (P written, one arrival per softmax warp), o (P.V
 // done: the buffer and O free again); at head_dim 128 also one per softmax
 // group for taking turns at the exponentials.  One barrier per buffer means
@@ -97,32 +98,6 @@ struct WsShape {
   static constexpr int kTmemUsed = kSCols + kQTiles * D;
   static constexpr int kTmemCols = kTmemUsed <= 256 ? 256 : 512;
 };
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-// arrive on `bar` and expect `bytes` more from bulk copies before its phase completes
-__device__ __forceinline__ void mbar_arrive_expect(uint64_t *bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-               "r"(bytes)
-               : "memory");
-}
-
-// 2D tile copy through a tensor map (128-byte swizzle), counted on `bar`;
-// x (elements) is a multiple of 64, so x * 2 bytes is 16-byte aligned
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
-                                            uint64_t *bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, "
-      "{%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -555,6 +530,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const bool empty = bad || l == 0.f || !have_o;
     const float inv = empty ? 0.f : 1.f / l;
+    // an empty or bad row stores exact zeros (a skipped tile can leave any bits in O)
+    auto scaled = [&](float x) { return empty ? 0.f : x * inv; };
     const size_t prow = orow * p.num_splits + split;  // used in the split read only
     if (partial && row_ok)
       p.partial_lse[prow] =
@@ -573,16 +550,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; e += 4)
           *reinterpret_cast<float4 *>(dst + e) =
-              make_float4(o[e] * inv, o[e + 1] * inv, o[e + 2] * inv, o[e + 3] * inv);
+              make_float4(scaled(o[e]), scaled(o[e + 1]), scaled(o[e + 2]), scaled(o[e + 3]));
       } else if (row_ok) {
         T *dst = static_cast<T *>(p.out) + orow * D + cb;
 #pragma unroll
         for (int e = 0; e < 32; e += 8) {
           uint4 w;
-          w.x = Pack2<T>::run(o[e] * inv, o[e + 1] * inv);
-          w.y = Pack2<T>::run(o[e + 2] * inv, o[e + 3] * inv);
-          w.z = Pack2<T>::run(o[e + 4] * inv, o[e + 5] * inv);
-          w.w = Pack2<T>::run(o[e + 6] * inv, o[e + 7] * inv);
+          w.x = Pack2<T>::run(scaled(o[e]), scaled(o[e + 1]));
+          w.y = Pack2<T>::run(scaled(o[e + 2]), scaled(o[e + 3]));
+          w.z = Pack2<T>::run(scaled(o[e + 4]), scaled(o[e + 5]));
+          w.w = Pack2<T>::run(scaled(o[e + 6]), scaled(o[e + 7]));
           *reinterpret_cast<uint4 *>(dst + e) = w;
         }
       }
@@ -620,15 +597,17 @@ EncodeTiled encoder() {
 
 // A 2D view of a pool: rows = num_pages * block_size token rows of Hkv * D
 // elements; a box is 64 elements (one 128-byte swizzle span) by
-// min(block_size, 64) rows, so one copy moves one kv head's rows of a page.
-bool make_pool_map(CUtensorMap *map, const void *pool, pa_dtype dtype, const ChunkParams &p) {
+// min(block_size, box_rows) rows, so one copy moves one kv head's rows of a
+// page (or of a key tile's part of a page).
+bool make_pool_map(CUtensorMap *map, const void *pool, pa_dtype dtype, const ChunkParams &p,
+                   int box_rows) {
   EncodeTiled enc = encoder();
   if (enc == nullptr) return false;
   const int bs = 1 << p.block_size_log2;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.num_kv_heads) * p.head_dim,
                               static_cast<cuuint64_t>(p.num_pages) * bs};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.num_kv_heads) * p.head_dim * 2};
-  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(bs < 64 ? bs : 64)};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(bs < box_rows ? bs : box_rows)};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = enc(map,
                          dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -644,11 +623,12 @@ bool make_pool_map(CUtensorMap *map, const void *pool, pa_dtype dtype, const Chu
 // (the pool's address, extents and dtype), valid in any context.
 struct MapKey {
   const void *pool;
-  int32_t num_pages, block_size_log2, num_kv_heads, head_dim;
+  int32_t num_pages, block_size_log2, num_kv_heads, head_dim, box_rows;
   pa_dtype dtype;
   bool operator==(const MapKey &o) const {
     return pool == o.pool && num_pages == o.num_pages && block_size_log2 == o.block_size_log2 &&
-           num_kv_heads == o.num_kv_heads && head_dim == o.head_dim && dtype == o.dtype;
+           num_kv_heads == o.num_kv_heads && head_dim == o.head_dim && box_rows == o.box_rows &&
+           dtype == o.dtype;
   }
 };
 constexpr int kMapCache = 16;
@@ -657,8 +637,12 @@ MapKey g_map_key[kMapCache];
 CUtensorMap g_map_val[kMapCache];
 int g_map_used = 0, g_map_next = 0;
 
-bool pool_map(CUtensorMap *map, const void *pool, pa_dtype dtype, const ChunkParams &p) {
-  const MapKey key{pool, p.num_pages, p.block_size_log2, p.num_kv_heads, p.head_dim, dtype};
+}  // namespace
+
+bool pool_tensor_map(CUtensorMap *map, const void *pool, pa_dtype dtype, const ChunkParams &p,
+                     int box_rows) {
+  const MapKey key{pool, p.num_pages, p.block_size_log2, p.num_kv_heads, p.head_dim, box_rows,
+                   dtype};
   {
     std::lock_guard<std::mutex> lock(g_map_mu);
     for (int i = 0; i < g_map_used; ++i)
@@ -667,7 +651,7 @@ bool pool_map(CUtensorMap *map, const void *pool, pa_dtype dtype, const ChunkPar
         return true;
       }
   }
-  if (!make_pool_map(map, pool, dtype, p)) return false;
+  if (!make_pool_map(map, pool, dtype, p, box_rows)) return false;
   std::lock_guard<std::mutex> lock(g_map_mu);
   const int i = g_map_used < kMapCache ? g_map_used++ : (g_map_next++ % kMapCache);
   g_map_key[i] = key;
@@ -682,6 +666,10 @@ bool pool_map(CUtensorMap *map, const void *pool, pa_dtype dtype, const ChunkPar
 // give up.  Off unless a test turns it on.
 std::atomic<int> g_withhold_tiles{0};
 
+int withhold_tiles() { return g_withhold_tiles.load(std::memory_order_relaxed); }
+
+namespace {
+
 template <typename T, int D>
 cudaError_t launch_d(const ChunkParams &p, pa_dtype dtype, cudaStream_t stream) {
   auto kern = chunk_tc_ws_kernel<T, D>;
@@ -691,9 +679,10 @@ cudaError_t launch_d(const ChunkParams &p, pa_dtype dtype, cudaStream_t stream) 
   // tensor-map copies need pages of at least 8 tokens (a 1024-byte swizzle
   // atom per copy); otherwise, or without an encoder, every tile uses cp.async
   CUtensorMap mk{}, mv{};
-  const int use_tma = p.block_size_log2 >= 3 && pool_map(&mk, p.k_pool, dtype, p) &&
-                      pool_map(&mv, p.v_pool, dtype, p);
-  const int withhold = g_withhold_tiles.load(std::memory_order_relaxed);
+  const int use_tma = p.block_size_log2 >= 3 &&
+                      pool_tensor_map(&mk, p.k_pool, dtype, p, kKeyTile) &&
+                      pool_tensor_map(&mv, p.v_pool, dtype, p, kKeyTile);
+  const int withhold = withhold_tiles();
   const int nblk = (p.chunk_len * p.group + kCtaRows - 1) / kCtaRows;
   dim3 grid(nblk * p.num_kv_heads, p.num_seqs, p.partial_out ? p.num_splits : 1);
   return launch_pdl(kern, grid, dim3(kThreads), smem, stream, p, mk, mv, use_tma, withhold);

@@ -3,6 +3,7 @@
 // the C-ABI layer before any launcher here is called.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -134,6 +135,18 @@ cudaError_t launch_chunk_tc(const ChunkParams &p, pa_dtype dtype, cudaStream_t s
 // warp-specialized tcgen05 chunk read (pa_chunk_tc_ws.cu): two 128-row Q tiles per CTA
 bool chunk_tc_ws_supports(pa_dtype dtype, int head_dim, int rows);
 cudaError_t launch_chunk_tc_ws(const ChunkParams &p, pa_dtype dtype, cudaStream_t stream);
+// pipelined tcgen05 chunk read (pa_chunk_tc_pipe.cu): one 128-row Q tile per CTA, S
+// double-buffered, several CTAs per SM
+bool chunk_tc_pipe_supports(pa_dtype dtype, int head_dim, int rows);
+cudaError_t launch_chunk_tc_pipe(const ChunkParams &p, pa_dtype dtype, cudaStream_t stream);
+// A 2D tensor map of a pool (token rows of Hkv * D elements, 128-byte swizzle) whose box
+// is 64 elements by min(block_size, box_rows) rows, from a small cache of encoded maps
+// (pa_chunk_tc_ws.cu); false when the driver's encoder is unavailable or refuses.
+bool pool_tensor_map(CUtensorMap *map, const void *pool, pa_dtype dtype, const ChunkParams &p,
+                     int box_rows);
+// State of the time-out test hook (pa_test_set_withhold_tiles): nonzero makes the
+// tcgen05 chunk reads' loaders announce no tile, so that their bounded waits run out.
+int withhold_tiles();
 cudaError_t launch_append(const AppendParams &p, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams &p, pa_dtype dtype, cudaStream_t stream);
 

@@ -4,6 +4,7 @@
 // swizzle of the K-major / MN-major tiles the tensor core reads.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -71,6 +72,32 @@ __device__ __forceinline__ void commit(uint32_t mbar) {
                : "memory");
 }
 
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// arrive on `bar` and expect `bytes` more from bulk copies before its phase completes
+__device__ __forceinline__ void mbar_arrive_expect(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// 2D tile copy through a tensor map (128-byte swizzle), counted on `bar`;
+// x (elements) is a multiple of 64, so x * 2 bytes is 16-byte aligned
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
+                                            uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Wait for the given phase of an mbarrier; false once the bounds above are
 // reached.  Each poll passes a 20 ns suspend hint (measured a few per cent
 // faster than the default limit).
@@ -114,6 +141,15 @@ __device__ __forceinline__ void wait_st_tied(uint32_t *q) {
 }
 
 __device__ __forceinline__ void tie32(uint32_t *q) { asm volatile("" : PA_TIE32(q)); }
+
+#define PA_TIE16(q)                                                                        \
+  "+r"(q[0]), "+r"(q[1]), "+r"(q[2]), "+r"(q[3]), "+r"(q[4]), "+r"(q[5]), "+r"(q[6]),      \
+      "+r"(q[7]), "+r"(q[8]), "+r"(q[9]), "+r"(q[10]), "+r"(q[11]), "+r"(q[12]),           \
+      "+r"(q[13]), "+r"(q[14]), "+r"(q[15])
+
+__device__ __forceinline__ void wait_st_tied16(uint32_t *q) {
+  asm volatile("tcgen05.wait::st.sync.aligned;" : PA_TIE16(q)::"memory");
+}
 
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
   uint32_t r[32];
@@ -183,6 +219,20 @@ __device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t *v) {
   wait_st_tied(q);
 }
 
+// 16 consecutive columns of this warp's 32 lanes from 16 packed words
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t *v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15]));
+  uint32_t q[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) q[j] = v[j];
+  wait_st_tied16(q);
+}
+
 template <typename T> struct Pack2;
 template <> struct Pack2<__nv_bfloat16> {
   __device__ __forceinline__ static uint32_t run(float lo, float hi) {
@@ -242,6 +292,45 @@ __device__ __forceinline__ float row_exp64(float *s, float sl2, float mu) {
   uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
   for (int c = 0; c < 32; ++c) {
+    uint64_t x;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(x) : "l"(pack_f2(s[2 * c], s[2 * c + 1])),
+        "l"(scale), "l"(shift));
+    float a, b;
+    unpack_f2(x, a, b);
+    a = ex2_approx(a);
+    b = ex2_approx(b);
+    s[2 * c] = a;
+    s[2 * c + 1] = b;
+    asm("add.rn.f32x2 %0, %0, %1;" : "+l"(acc[c & 3]) : "l"(pack_f2(a, b)));
+  }
+  float t[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) unpack_f2(acc[i], t[2 * i], t[2 * i + 1]);
+  return ((t[0] + t[1]) + (t[2] + t[3])) + ((t[4] + t[5]) + (t[6] + t[7]));
+}
+
+// The same two pieces on N scores (N a multiple of 8).
+template <int N>
+__device__ __forceinline__ float row_max_n(const float *s) {
+  float r[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float m = s[i];
+    int c = i + 8;
+#pragma unroll
+    for (; c + 8 < N; c += 16) m = max3(m, s[c], s[c + 8]);
+    if (c < N) m = fmaxf(m, s[c]);
+    r[i] = m;
+  }
+  return max3(max3(r[0], r[1], r[2]), max3(r[3], r[4], r[5]), fmaxf(r[6], r[7]));
+}
+
+template <int N>
+__device__ __forceinline__ float row_exp_n(float *s, float sl2, float mu) {
+  const uint64_t scale = pack_f2(sl2, sl2), shift = pack_f2(-mu, -mu);
+  uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+  for (int c = 0; c < N / 2; ++c) {
     uint64_t x;
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(x) : "l"(pack_f2(s[2 * c], s[2 * c + 1])),
         "l"(scale), "l"(shift));

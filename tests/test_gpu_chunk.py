@@ -309,11 +309,12 @@ def test_small_chunks_on_the_decode_kernel(lib, dtype, hq, hkv, d, bs, n_q, lens
     assert_attn_close(out, _ref(base, q), base.dtype)
 
 
-def test_warp_specialized_wait_time_out_is_reported(lib):
-    # the load warps announce no key tile (test hook), so the MMA and softmax waits run
+@pytest.mark.parametrize("n_q", [16, 64])   # 64 rows: pipelined kernel; 256: two Q tiles
+def test_warp_specialized_wait_time_out_is_reported(lib, n_q):
+    # the load warp(s) announce no key tile (test hook), so the MMA and softmax waits run
     # out; the call reports PA_DEV_TIMEOUT, zeroes its outputs and leaves the context usable
     base = workloads.make_batch("wstimeout", 50, "bf16", [300], 4, 1, 64, 16, 30)
-    q = _chunk_batch(base, 64)                  # 64 queries x 4 heads = 256 rows: one CTA
+    q = _chunk_batch(base, n_q)                 # one CTA either way
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     lib.pa_test_set_withhold_tiles(True)
     try:
