@@ -951,8 +951,9 @@ def chunk_longctx(pa, workloads, torch, dev, peak, flush):
 def launch_floor(pa, workloads, torch, dev, peak):
     """The read's fixed cost per launch at history 1024 (B 64): the same batch with every
     length 0 (the same 512-CTA grid, reading only q and the lengths) beside the real read,
-    and two events with nothing between them, each after an L2 flush.  Launch order (for an
-    ncu capture of decode_mma): 3 + 30 empty reads, then 3 + 30 real ones."""
+    and two events with nothing between them, each after an L2 flush; then the read in a
+    loop of back-to-back launches.  Launch order (for an ncu capture of decode_mma): 3 + 30
+    empty reads, then 3 + 30 real ones, then 60 warm-up and 20 timed loop launches."""
     flush = L2Flush(torch, dev)
     g = workloads.llama1b(1024, device=str(dev))
     out = torch.empty_like(g.q)
@@ -966,9 +967,36 @@ def launch_floor(pa, workloads, torch, dev, peak):
     detail = {"us_events_alone": 1e3 * n_med, "us_empty_read": 1e3 * e_med,
               "us_read_h1024": 1e3 * r_med, "us_read_h1024_min": 1e3 * r_min,
               "frac_read_h1024": rb / (r_med * 1e-3) / 1e9 / peak}
-    del g, out
+    # A decode loop: the read launched back to back, as a serving step issues it, on two
+    # batches in turn (their K/V, 2 x 134.5 MB, exceed L2, so each read comes from DRAM).
+    # The timed loop lies between cudaProfilerStart and cudaProfilerStop, so that an ncu
+    # range replay (--replay-mode range --profile-from-start off) measures exactly it.
+    g2 = workloads.make_batch("llama1b_h1024_second", seed=5, dtype="bf16", lens=[1024] * 64,
+                              num_q_heads=32, num_kv_heads=8, head_dim=64, block_size=16,
+                              num_pages=20000, device=str(dev))
+    out2 = torch.empty_like(g2.q)
+    real2 = lambda: pa.pa_decode(out2, g2.q, g2.k_pool, g2.v_pool, g2.block_table,
+                                 g2.seq_lens, g2.scale)
+    n_loop = 20
+    for _ in range(3):
+        for i in range(n_loop):
+            (real if i % 2 == 0 else real2)()
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.profiler.start()
+    start.record()
+    for i in range(n_loop):
+        (real if i % 2 == 0 else real2)()
+    stop.record()
+    torch.cuda.profiler.stop()
+    torch.cuda.synchronize()
+    loop_us = 1e3 * start.elapsed_time(stop) / n_loop
+    detail.update({"us_read_h1024_in_loop": loop_us, "loop_launches": n_loop,
+                   "frac_read_h1024_in_loop": rb / (loop_us * 1e-6) / 1e9 / peak})
+    del g, out, g2, out2
     torch.cuda.empty_cache()
-    return {k: detail[k] for k in ("us_empty_read", "us_read_h1024")}, detail
+    return {k: detail[k] for k in ("us_empty_read", "us_read_h1024",
+                                   "us_read_h1024_in_loop")}, detail
 
 
 def f32_read(pa, workloads, torch, dev, peak):
