@@ -394,13 +394,14 @@ __global__ void __launch_bounds__(kThreads, PipeShape<D>::kMinBlocks)
         if (!wait_phase(smem_u32(&bar_o[(j - 1) & 1]), ((j - 1) >> 1) & 1)) fail = true;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         if (!__any_sync(0xffffffffu, fail)) {
+          // 16 columns at a time (32 would spill under this kernel's register bound)
 #pragma unroll
-          for (int cb = 0; cb < D; cb += 32) {
-            float o[32];
-            tmem_ld32(t_o + cb, o);
+          for (int cb = 0; cb < D; cb += 16) {
+            uint32_t o[16];
+            tmem_ld16u(t_o + cb, o);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] *= alpha;
-            tmem_st32(t_o + cb, o);
+            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st16u(t_o + cb, o);
           }
         }
       }

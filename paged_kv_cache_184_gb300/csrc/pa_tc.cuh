@@ -219,6 +219,18 @@ __device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t *v) {
   wait_st_tied(q);
 }
 
+// 16 consecutive columns of this warp's 32 lanes into 16 words
+__device__ __forceinline__ void tmem_ld16u(uint32_t taddr, uint32_t *q) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16];"
+      : "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3]), "=r"(q[4]), "=r"(q[5]), "=r"(q[6]),
+        "=r"(q[7]), "=r"(q[8]), "=r"(q[9]), "=r"(q[10]), "=r"(q[11]), "=r"(q[12]), "=r"(q[13]),
+        "=r"(q[14]), "=r"(q[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : PA_TIE16(q)::"memory");
+}
+
 // 16 consecutive columns of this warp's 32 lanes from 16 packed words
 __device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t *v) {
   asm volatile(
