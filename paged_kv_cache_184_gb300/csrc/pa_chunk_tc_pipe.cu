@@ -508,12 +508,15 @@ cudaError_t launch_t(const ChunkParams &p, pa_dtype dtype, cudaStream_t stream) 
 
 }  // namespace
 
-// Head_dim 64 from 64 rows per (sequence, kv head).  At head_dim 128 (two CTAs
-// per SM, two 64-token stages) the single-tile kernel measured faster: 990 against
-// 1252 us for 32-query chunks on 8 x 32,768-token histories.
+// Head_dim 64 from 17 rows per (sequence, kv head), everything past the decode
+// kernel's chunk mode (16 columns).  Below 64 rows it replaced the mma.sync chunk
+// kernel: 24 / 32 / 48 rows (6 / 8 / 12 queries of the 64 x 4096-token batch) took
+// 102.6 / 102.9 / 106.1 us here against 115.2 / 115.5 / 136.0 there.  At head_dim
+// 128 (two CTAs per SM, two 64-token stages) the single-tile kernel measured
+// faster: 990 against 1252 us for 32-query chunks on 8 x 32,768-token histories.
 bool chunk_tc_pipe_supports(pa_dtype dtype, int head_dim, int rows) {
   if (dtype != PA_F16 && dtype != PA_BF16) return false;
-  return head_dim == 64 && rows >= kRows / 2;
+  return head_dim == 64 && rows >= 17;
 }
 
 cudaError_t launch_chunk_tc_pipe(const ChunkParams &p, pa_dtype dtype, cudaStream_t stream) {
