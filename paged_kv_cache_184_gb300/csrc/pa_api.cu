@@ -250,16 +250,15 @@ pa_status pa_decode_work(float *partial_out, float *partial_lse, const int32_t *
 
 // The chunk read for this many (query, head) rows per kv head: warp-specialized
 // tcgen05 with two Q tiles per CTA for chunks of two full 128-row tiles or more;
-// below that the pipelined one-tile tcgen05 read at head_dim 64 (every chunk that
-// reaches here: the decode kernel takes up to 16 columns), the single-tile tcgen05
-// read from 128 rows at head_dim 128; mma.sync for the rest.
+// below that the pipelined one-tile tcgen05 read at head_dim 64 and 128 (every
+// chunk that reaches here: the decode kernel takes up to 16 columns at 64, 8 at
+// 128); mma.sync at the other head dims.
 static cudaError_t launch_chunk_read(const pa::ChunkParams &p, pa_dtype dtype, int64_t rows,
                                      cudaStream_t s) {
   const int r = static_cast<int>(rows);
   if (pa::chunk_tc_ws_supports(dtype, p.head_dim, r)) return pa::launch_chunk_tc_ws(p, dtype, s);
   if (pa::chunk_tc_pipe_supports(dtype, p.head_dim, r))
     return pa::launch_chunk_tc_pipe(p, dtype, s);
-  if (pa::chunk_tc_supports(dtype, p.head_dim, r)) return pa::launch_chunk_tc(p, dtype, s);
   return pa::launch_chunk(p, dtype, s);
 }
 

@@ -4,14 +4,13 @@
 // Same contract as the other chunk reads (nanoserve "Day 23: the real
 // triton.jit paged-attention kernel": query i of a chunk sits at position
 // past + i and sees tokens 0 .. past + i) and the same per-row arithmetic as
-// chunk_tc_kernel (fp32 online softmax with a lazily moved reference max, P
-// rounded to the cache dtype).  It serves chunks of 64-255 (query, head) rows
-// per kv head: too few rows for two Q tiles per CTA, so several CTAs share an
-// SM and each keeps its own K/V stream going.
+// the warp-specialized read (fp32 online softmax with a lazily moved
+// reference max, P rounded to the cache dtype).  It serves chunks of up to 255
+// (query, head) rows per kv head: too few rows for two Q tiles per CTA, so
+// several CTAs share an SM and each keeps its own K/V stream going.
 //
-// In the single-tile kernel every key tile runs QK, a tensor-memory round
-// trip, the softmax, and P.V with another round trip, one after the other.
-// Here:
+// Run in order, every key tile costs QK, a tensor-memory round trip, the
+// softmax, and P.V with another round trip.  Here the phases overlap:
 //
 //   warps 0-3   softmax: thread r owns row r (tensor-memory lane r), reads its
 //               S row, writes its P row back over S as 16-bit pairs, and moves
@@ -29,14 +28,13 @@
 //               mbarrier), a ragged last tile (or pages of fewer than 8
 //               tokens) by 16-byte cp.async with zero-fill
 //
-// Tensor memory: S_0 | S_1 (KT columns each) | O (D columns).  At head_dim
-// 64 the key tile is 32 tokens, so the three take 128 columns and four CTAs
-// (49 KB of shared memory each) share an SM; a 128 x 32 x 16 product costs
-// the tensor pipe about as long as a 128 x 64 x 16 one (~50 cycles), so QK
-// takes twice the pipe time per key, which the pipe has to spare here.  The
-// kernel is written for any head_dim that is a multiple of 64 (64-token tiles
-// and 256 columns at 128), but only head_dim 64 is built: at 128, with two CTAs
-// per SM and two stages, the single-tile kernel measured faster.
+// Tensor memory: S_0 | S_1 (32 columns each) | O (head_dim columns).  Key
+// tiles are 32 tokens so that at head_dim 64 the three take 128 columns and
+// four CTAs (49 KB of shared memory each) share an SM; at head_dim 128 they
+// take 192 (256 allocated) and two CTAs (97 KB each) share one.  A 128 x 32 x
+// 16 product costs the tensor pipe about as long as a 128 x 64 x 16 one (~50
+// cycles, measured), so QK takes twice the pipe time per key that 64-token
+// tiles would; with four CTAs per SM the pipe still has room.
 //
 // mbarriers: full/empty per ring stage, and per S buffer s (S ready), p (P
 // written, one arrival per live softmax warp) and o (P.V done: buffer and O
@@ -71,6 +69,9 @@ constexpr float kRescaleLog2 = 8.f;
 template <int D> struct PipeShape;
 template <> struct PipeShape<64> {
   static constexpr int kKeyTile = 32, kStages = 4, kMinBlocks = 4;
+};
+template <> struct PipeShape<128> {
+  static constexpr int kKeyTile = 32, kStages = 4, kMinBlocks = 2;
 };
 
 template <int D>
@@ -503,19 +504,24 @@ cudaError_t launch_d(const ChunkParams &p, pa_dtype dtype, cudaStream_t stream) 
 template <typename T>
 cudaError_t launch_t(const ChunkParams &p, pa_dtype dtype, cudaStream_t stream) {
   if (p.head_dim == 64) return launch_d<T, 64>(p, dtype, stream);
+  if (p.head_dim == 128) return launch_d<T, 128>(p, dtype, stream);
   return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-// Head_dim 64 from 17 rows per (sequence, kv head), everything past the decode
-// kernel's chunk mode (16 columns).  Below 64 rows it replaced the mma.sync chunk
-// kernel: 24 / 32 / 48 rows (6 / 8 / 12 queries of the 64 x 4096-token batch) took
-// 102.6 / 102.9 / 106.1 us here against 115.2 / 115.5 / 136.0 there.  At head_dim
-// 128 (two CTAs per SM, two 64-token stages) the single-tile kernel measured
-// faster: 990 against 1252 us for 32-query chunks on 8 x 32,768-token histories.
+// Every chunk past the decode kernel's chunk mode (16 columns at head_dim 64, 8
+// at 128) and below two Q tiles.  It replaced the mma.sync chunk kernel below 64
+// (head_dim 64) and 128 (head_dim 128) rows, and a one-tile tcgen05 kernel that
+// ran each key tile's phases in order above: at head_dim 64, 24 / 32 / 48 / 64
+// rows (6 / 8 / 12 / 16 queries of the 64 x 4096-token batch) took 104.4 / 104.7
+// / 106.8 / 107.8 us against 115.3 / 116.4 / 137.2 / 129.2; at head_dim 128, the
+// 8 x 32,768-token batch in 64-page splits took 227 / 256 / 281 / 308 us at 4 / 16
+// / 24 / 32 queries against 238 / 297 / 550 / 344, one pass of 32 queries 810
+// against 992 us.
 bool chunk_tc_pipe_supports(pa_dtype dtype, int head_dim, int rows) {
   if (dtype != PA_F16 && dtype != PA_BF16) return false;
+  if (head_dim == 128) return rows >= 9;
   return head_dim == 64 && rows >= 17;
 }
 

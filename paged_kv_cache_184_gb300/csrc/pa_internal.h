@@ -127,10 +127,6 @@ cudaError_t launch_decode_items(const DecodeParams &p, pa_dtype dtype, cudaStrea
 bool chunk_supports(pa_dtype dtype, int head_dim);
 int chunk_rows_per_cta();
 cudaError_t launch_chunk(const ChunkParams &p, pa_dtype dtype, cudaStream_t stream);
-// Its tcgen05 variant, for at least one full 128-row tile per (sequence, kv head):
-// f16/bf16, head_dim 64 or 128.
-bool chunk_tc_supports(pa_dtype dtype, int head_dim, int rows);
-cudaError_t launch_chunk_tc(const ChunkParams &p, pa_dtype dtype, cudaStream_t stream);
 
 // warp-specialized tcgen05 chunk read (pa_chunk_tc_ws.cu): two 128-row Q tiles per CTA
 bool chunk_tc_ws_supports(pa_dtype dtype, int head_dim, int rows);

@@ -137,7 +137,7 @@ def test_tensor_core_chunks(lib, dtype, hq, hkv, d, bs, n_q, lens):
     assert_attn_close(out, _ref(base, q), base.dtype)
 
 
-# 64-128 (query, head) rows per kv head at head_dim 64 (the single-tile tcgen05 read):
+# 64-128 (query, head) rows per kv head at head_dim 64 (the pipelined one-tile tcgen05 read):
 # an empty sequence, lengths far apart, odd (sequence, kv head) counts, odd page sizes
 @pytest.mark.parametrize("dtype,hq,hkv,bs,n_q,lens", [
     ("bf16", 12, 3, 16, 16, [0, 16, 4000, 1500, 77]),      # 15 (sequence, kv head) pairs
@@ -331,7 +331,7 @@ def test_warp_specialized_wait_time_out_is_reported(lib, n_q):
     assert_attn_close(out, _ref(base, q), base.dtype)
 
 
-@pytest.mark.parametrize("n_q", [40, 80])        # 160 rows: single-tile kernel; 320: warp-specialized
+@pytest.mark.parametrize("n_q", [40, 80])        # 160 rows: one Q tile per CTA; 320: two
 def test_tensor_core_bad_seq_len_is_reported_and_zeroed(lib, n_q):
     base = workloads.make_batch("tclen", 51, "bf16", [100, 300], 32, 8, 64, 16, 40)
     q = _chunk_batch(base, n_q)

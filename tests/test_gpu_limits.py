@@ -6,8 +6,8 @@ call at such a limit, compared element by element with the fp64 oracle:
 
 * block_size 1024 on every read path: the single-pass read (tensor-core and
   CUDA-core), the split read + merge, and the chunked read on each of its
-  kernels (the decode kernel's chunk mode, mma.sync, single-tile and
-  warp-specialized tcgen05) and its split form;
+  kernels (the decode kernel's chunk mode, the pipelined one-tile and the
+  warp-specialized tcgen05 reads) and its split form;
 * 65,535 sequences of short histories, single pass and split + merge;
 * merges over 20,000+ splits: one sequence of 327,680 tokens split into
   one-page runs (through the split read), and random partials with empty
@@ -100,7 +100,8 @@ def test_block_size_1024_single_pass_and_split(lib, dtype, hq, hkv, d):
 @pytest.mark.parametrize("d,n_q", [(64, 4), (64, 8), (64, 32), (64, 64), (128, 2), (128, 64)])
 def test_block_size_1024_chunked_read_and_its_splits(lib, d, n_q):
     # G = 4: n_q * 4 rows per kv head reach the decode kernel's chunk mode (<= 16 at head_dim
-    # 64, <= 8 at 128), mma.sync (32), single-tile tcgen05 (128) and warp-specialized (256)
+    # 64, <= 8 at 128), the pipelined one-tile tcgen05 read (32, 128) and the warp-specialized
+    # one (256)
     lens = [max(n_q, x) for x in (70, 1023, 1024, 1025, 2500)]
     pages = sum(-(-n // 1024) for n in lens) + 2
     g = workloads.make_batch("bs1024c", 72, "bf16", lens, 16, 4, d, 1024, pages).to(DEV)
