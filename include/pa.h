@@ -253,8 +253,9 @@ pa_status pa_decode_work(float *partial_out, float *partial_lse, const int32_t *
  * one query, or of up to 16 (query, head) columns per kv head at head_dim 64
  * (8 at head_dim 128), run on the single-query read's kernel with a causal
  * limit per column; larger ones at head_dim 64 and 128 on the tcgen05
- * tensor cores (warp-specialized with two Q tiles from 256 rows); the other
- * head dims on the mma.sync chunk kernel.
+ * tensor cores (two Q tiles per CTA from 256 rows, except head_dim-64 chunks
+ * longer than an eighth of the table's capacity); the other head dims on the
+ * mma.sync chunk kernel.
  * chunk_len * (num_q_heads / num_kv_heads) above 2^30 (query, head) rows
  * per kv head returns PA_ERR_UNSUPPORTED.
  *

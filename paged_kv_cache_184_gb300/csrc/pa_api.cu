@@ -248,15 +248,23 @@ pa_status pa_decode_work(float *partial_out, float *partial_lse, const int32_t *
   return launched(pa::launch_decode_items(p, dtype, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-// The chunk read for this many (query, head) rows per kv head: warp-specialized
-// tcgen05 with two Q tiles per CTA for chunks of two full 128-row tiles or more;
-// below that the pipelined one-tile tcgen05 read at head_dim 64 and 128 (every
-// chunk that reaches here: the decode kernel takes up to 16 columns at 64, 8 at
-// 128); mma.sync at the other head dims.
+// The chunk read for this many (query, head) rows per kv head.  From 256 rows
+// (two full 128-row tiles) the warp-specialized tcgen05 read with two Q tiles per
+// CTA, except at head_dim 64 when the chunk is more than an eighth of the table's
+// capacity (a prefill, say): there the pipelined one-tile read, four CTAs per SM,
+// measured faster (prefills of 8 x 4096 / 32 x 1024 / 64 x 512 tokens: 786 / 289
+// / 213 us against 842 / 377 / 299), while on a short chunk of a long history the
+// two Q tiles sharing each K/V load pay (128 queries at history 4096: 383 against
+// 411 us).  Below 256 rows the pipelined read at head_dim 64 and 128 (every chunk
+// that reaches here: the decode kernel takes up to 16 columns at 64, 8 at 128);
+// mma.sync at the other head dims.
 static cudaError_t launch_chunk_read(const pa::ChunkParams &p, pa_dtype dtype, int64_t rows,
                                      cudaStream_t s) {
   const int r = static_cast<int>(rows);
-  if (pa::chunk_tc_ws_supports(dtype, p.head_dim, r)) return pa::launch_chunk_tc_ws(p, dtype, s);
+  const long long capacity = static_cast<long long>(p.max_blocks) << p.block_size_log2;
+  const bool long_chunk = static_cast<long long>(p.chunk_len) * 8 > capacity;
+  if (pa::chunk_tc_ws_supports(dtype, p.head_dim, r) && !(p.head_dim == 64 && long_chunk))
+    return pa::launch_chunk_tc_ws(p, dtype, s);
   if (pa::chunk_tc_pipe_supports(dtype, p.head_dim, r))
     return pa::launch_chunk_tc_pipe(p, dtype, s);
   return pa::launch_chunk(p, dtype, s);

@@ -200,23 +200,24 @@ def test_tensor_core_bad_page_is_reported_and_zeroed(lib):
     assert_attn_close(out[:2], _ref(base, q, [0, 1]), base.dtype)
 
 
-def test_prefill_4096_whole_prompt_and_sampled_rows(lib):
-    # the measured prefill launch (8 prompts x 4096 tokens, head_dim 128): one whole prompt
-    # (every query and head) against the oracle's chunked read, and sampled queries of two
-    # more prompts against attention over their causal prefixes
-    base = workloads.make_batch("prefill_d128", 6, "bf16", [4096] * 8, 32, 8, 128, 16, 8 * 256,
+@pytest.mark.parametrize("d", [64, 128])   # the pipelined one-tile read; two Q tiles per CTA
+def test_prefill_4096_whole_prompt_and_sampled_rows(lib, d):
+    # the measured prefill launch (8 prompts x 4096 tokens): one whole prompt (every query
+    # and head) against the oracle's chunked read, and sampled queries of two more prompts
+    # against attention over their causal prefixes
+    base = workloads.make_batch(f"prefill_d{d}", 6, "bf16", [4096] * 8, 32, 8, d, 16, 8 * 256,
                                 device=DEV)
     gen = torch.Generator(device=DEV)
     gen.manual_seed(8)
-    q = torch.randn((8, 4096, 32, 128), generator=gen, device=DEV).to(torch.bfloat16)
+    q = torch.randn((8, 4096, 32, d), generator=gen, device=DEV).to(torch.bfloat16)
     out = torch.empty_like(q)
     lib.pa_decode_chunk(out, q, base.k_pool, base.v_pool, base.block_table, base.seq_lens,
                         base.scale)
     torch.cuda.synchronize()
     for b in (0, 7):
         pages = base.block_table[b].long()
-        k = host_f32(base.k_pool.index_select(0, pages)).reshape(4096, 8, 128)
-        v = host_f32(base.v_pool.index_select(0, pages)).reshape(4096, 8, 128)
+        k = host_f32(base.k_pool.index_select(0, pages)).reshape(4096, 8, d)
+        v = host_f32(base.v_pool.index_select(0, pages)).reshape(4096, 8, d)
         for i in (0, 1, 127, 128, 2000, 4095):
             for h in (0, 5, 31):
                 ref, _ = oracle.attend(host_f32(q[b, i, h]), k[:i + 1, h // 4], v[:i + 1, h // 4],
@@ -226,9 +227,9 @@ def test_prefill_4096_whole_prompt_and_sampled_rows(lib):
     # time on float64 copies of the prompt's pages (heads are independent in the definition)
     b = 3
     pages = base.block_table[b].long()
-    kp = base.k_pool.index_select(0, pages).double().cpu().numpy()     # [256, 16, 8, 128]
+    kp = base.k_pool.index_select(0, pages).double().cpu().numpy()     # [256, 16, 8, d]
     vp = base.v_pool.index_select(0, pages).double().cpu().numpy()
-    qb = q[b:b + 1].double().cpu().numpy()                              # [1, 4096, 32, 128]
+    qb = q[b:b + 1].double().cpu().numpy()                              # [1, 4096, 32, d]
     got = out[b:b + 1]
     for g in range(8):
         ref = oracle.paged_decode_chunk(np.ascontiguousarray(qb[:, :, 4 * g:4 * g + 4]),
