@@ -360,25 +360,43 @@ __global__ void __launch_bounds__(kThreads, PipeShape<D>::kMinBlocks)
       const uint32_t t_s = tmem + (j & 1) * KT + t_lane;
       const int tok0 = t_lo + j * KT;
       float s[KT];
-      if constexpr (KT == 32) {
-        tmem_ld32(t_s, s);
-      } else {
-        tmem_ld64(t_s, s);
-      }
-      if (tok0 + KT - 1 > pos) {  // the tile crosses this row's last key
+      // S row of this thread, -inf past its last key (warp-collective load)
+      auto load_s = [&]() {
+        if constexpr (KT == 32) {
+          tmem_ld32(t_s, s);
+        } else {
+          tmem_ld64(t_s, s);
+        }
+        if (tok0 + KT - 1 > pos) {  // the tile crosses this row's last key
 #pragma unroll
-        for (int c = 0; c < KT; ++c)
-          if (tok0 + c > pos) s[c] = -CUDART_INF_F;
+          for (int c = 0; c < KT; ++c)
+            if (tok0 + c > pos) s[c] = -CUDART_INF_F;
+        }
+      };
+      load_s();
+      // Common case first: exponents against the current reference.  When their
+      // sum is at most 2^8 no probability exceeds 2^8, so the lazy rule would not
+      // move the reference and the row max is not needed (the result is the same
+      // bit for bit).  Otherwise, or before the first reference, the warp
+      // reloads S and takes the rule.
+      float alpha = 1.f, sum = 0.f;
+      bool full = m_ref == -CUDART_INF_F;
+      const bool tried = !__any_sync(0xffffffffu, full);
+      if (tried) {
+        sum = row_exp_n<KT>(s, sl2, m_ref * sl2);
+        full = !(sum <= 256.f);
       }
-      const float mx = row_max_n<KT>(s);
-      float alpha = 1.f;
-      if (mx != -CUDART_INF_F &&
-          (m_ref == -CUDART_INF_F || (mx - m_ref) * sl2 > kRescaleLog2)) {
-        alpha = m_ref == -CUDART_INF_F ? 0.f : ex2_approx((m_ref - mx) * sl2);
-        m_ref = mx;
+      if (__any_sync(0xffffffffu, full)) {
+        if (tried) load_s();  // the attempt overwrote s
+        const float mx = row_max_n<KT>(s);
+        if (mx != -CUDART_INF_F &&
+            (m_ref == -CUDART_INF_F || (mx - m_ref) * sl2 > kRescaleLog2)) {
+          alpha = m_ref == -CUDART_INF_F ? 0.f : ex2_approx((m_ref - mx) * sl2);
+          m_ref = mx;
+        }
+        const float mu = m_ref == -CUDART_INF_F ? 0.f : m_ref * sl2;
+        sum = row_exp_n<KT>(s, sl2, mu);  // masked: 2^-inf = 0
       }
-      const float mu = m_ref == -CUDART_INF_F ? 0.f : m_ref * sl2;
-      const float sum = row_exp_n<KT>(s, sl2, mu);  // masked: 2^-inf = 0
       l = fmaf(l, alpha, sum);
       {
         uint32_t w[KT / 2];
