@@ -193,29 +193,29 @@ __global__ void __launch_bounds__(kThreads, PipeShape<D>::kMinBlocks)
   if (warp == kLoadWarp) {
     // ------------------------------------------------------------ load warp
     // Tile j goes to stage j % kStages once P.V(j - kStages) has released it.
-    // Lane l holds the ids of pages first + l and first + 32 + l of its tile
-    // (read one tile ahead); an id outside the pool is reported, marks the
-    // outputs bad and reads as -1 (no copy).
+    // Lane l holds the id of page first + l of its tile (a 32-token tile spans
+    // at most 32 pages), read one tile ahead; an id outside the pool is
+    // reported, marks the outputs bad and reads as -1 (no copy).
     const int32_t *bt_row = p.block_table + static_cast<size_t>(b) * p.max_blocks;
     const T *kpool = static_cast<const T *>(p.k_pool);
     const T *vpool = static_cast<const T *>(p.v_pool);
-    auto fetch_pages = [&](int j, int &pa, int &pb) {
-      pa = pb = -1;
+    static_assert(KT == 32, "one page id per lane");
+    auto fetch_page = [&](int j) -> int {
+      int pa = -1;
       if (j < ntiles) {
         const int t0 = t_lo + j * KT;
         const int first = t0 >> bs_log2;
         const int last = (min(t0 + KT, kv_end) - 1) >> bs_log2;  // < max_blocks
-        if (first + lane <= last) pa = __ldg(bt_row + first + lane);
-        if (KT > 32 && first + 32 + lane <= last) pb = __ldg(bt_row + first + 32 + lane);
-        const bool bad_a = first + lane <= last && (pa < 0 || pa >= p.num_pages);
-        const bool bad_b = KT > 32 && first + 32 + lane <= last && (pb < 0 || pb >= p.num_pages);
-        if (bad_a || bad_b) {
-          report_error(p.dev_err, PA_DEV_BAD_PAGE);
-          s_bad = 1;
-          if (bad_a) pa = -1;
-          if (bad_b) pb = -1;
+        if (first + lane <= last) {
+          pa = __ldg(bt_row + first + lane);
+          if (pa < 0 || pa >= p.num_pages) {
+            report_error(p.dev_err, PA_DEV_BAD_PAGE);
+            s_bad = 1;
+            pa = -1;
+          }
         }
       }
+      return pa;
     };
     // one lane waits, the warp follows its answer (keeps the warp converged)
     auto warp_wait = [&](uint64_t *bar, uint32_t phase) -> bool {
@@ -223,8 +223,7 @@ __global__ void __launch_bounds__(kThreads, PipeShape<D>::kMinBlocks)
       if (lane == 0) ok = wait_phase(smem_u32(bar), phase) ? 1 : 0;
       return __shfl_sync(0xffffffffu, ok, 0) != 0;
     };
-    int pa, pb;
-    fetch_pages(0, pa, pb);
+    int pa = fetch_page(0);
     // test hook: no tile is ever announced, so the other roles' waits run out
     for (int j = 0; j < ntiles && !withhold; ++j) {
       const int st = j % kStages;
@@ -236,11 +235,10 @@ __global__ void __launch_bounds__(kThreads, PipeShape<D>::kMinBlocks)
       unsigned char *vs = ks + S::kKVBytes;
       const int t0 = t_lo + j * KT;
       const int first = t0 >> bs_log2;
-      int na, nb;
-      fetch_pages(j + 1, na, nb);
+      const int na = fetch_page(j + 1);
       if (use_tma && t0 + KT <= kv_end) {
         // pages of the tile: KT / bs of them (bs < KT), or one KT-row part of a page
-        const int rows = bs_log2 >= (KT == 64 ? 6 : 5) ? KT : (1 << bs_log2);
+        const int rows = bs_log2 >= 5 ? KT : (1 << bs_log2);
         const int npg = KT / rows;  // <= KT / 8 (bs >= 8)
         int pg[KT / 8];
 #pragma unroll
@@ -265,7 +263,6 @@ __global__ void __launch_bounds__(kThreads, PipeShape<D>::kMinBlocks)
         }
         __syncwarp();
         pa = na;
-        pb = nb;
         continue;
       }
 #pragma unroll 4
@@ -273,9 +270,7 @@ __global__ void __launch_bounds__(kThreads, PipeShape<D>::kMinBlocks)
         const int tr = idx / (D / 8), c = idx % (D / 8);
         const int t = t0 + tr;
         const int pi = (t >> bs_log2) - first;  // 0 .. KT - 1
-        const int pg_a = __shfl_sync(0xffffffffu, pa, pi & 31);
-        const int pg_b = __shfl_sync(0xffffffffu, pb, pi & 31);
-        const int page = pi < 32 ? pg_a : pg_b;
+        const int page = __shfl_sync(0xffffffffu, pa, pi);
         const bool valid = t < kv_end && page >= 0;
         const size_t off =
             valid ? (((static_cast<size_t>(page) << bs_log2) + (t & bs_mask)) * hkv + g) * D + c * 8
@@ -286,7 +281,6 @@ __global__ void __launch_bounds__(kThreads, PipeShape<D>::kMinBlocks)
       }
       cp_async_commit();
       pa = na;
-      pb = nb;
       cp_async_wait_all();
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor core
       __syncwarp();
