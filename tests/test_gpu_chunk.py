@@ -158,6 +158,27 @@ def test_chunks_of_64_to_128_rows(lib, dtype, hq, hkv, bs, n_q, lens):
     assert_attn_close(out, _ref(base, q), base.dtype)
 
 
+# 9-255 rows per kv head at head_dim 128 (the pipelined one-tile read): pages smaller than,
+# equal to and larger than its 32-token key tile, an empty and a one-token sequence
+@pytest.mark.parametrize("dtype,hq,hkv,bs,n_q,lens", [
+    ("bf16", 32, 8, 16, 16, [0, 16, 900, 2049]),            # 64 rows, pages of 16
+    ("f16", 32, 8, 64, 24, [24, 25, 700, 1500]),            # 96 rows, pages of 64
+    ("bf16", 16, 4, 1024, 30, [30, 1, 1100, 2050]),         # 120 rows, pages of 1024
+    ("bf16", 32, 8, 4, 5, [5, 40, 333, 777]),               # 20 rows, pages of 4 (cp.async)
+    ("f16", 32, 8, 32, 40, [40, 64, 500, 1600]),            # 160 rows, pages of 32: two Q tiles
+])
+def test_pipelined_chunks_at_head_dim_128(lib, dtype, hq, hkv, bs, n_q, lens):
+    pages = sum(-(-n // bs) for n in lens) + 5
+    base = workloads.make_batch("pipe128", 48, dtype, lens, hq, hkv, 128, bs, pages)
+    assert 9 <= n_q * (hq // hkv) < 256
+    q = _chunk_batch(base, n_q)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = _run(lib, base, q, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_attn_close(out, _ref(base, q), base.dtype)
+
+
 def test_chunk_of_64_rows_bad_page_zeroes_only_its_sequence(lib):
     # one kv head, 16 queries x 4 heads; only sequence 0's table is bad
     base = workloads.make_batch("pairbad", 47, "bf16", [500, 700, 300], 4, 1, 64, 16, 120)
