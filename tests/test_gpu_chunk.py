@@ -159,13 +159,17 @@ def test_chunks_of_64_to_128_rows(lib, dtype, hq, hkv, bs, n_q, lens):
 
 
 # 9-255 rows per kv head at head_dim 128 (the pipelined one-tile read): pages smaller than,
-# equal to and larger than its 32-token key tile, an empty and a one-token sequence
+# equal to and larger than its 32-token key tile, an empty and a one-token sequence, odd
+# and single kv-head counts
 @pytest.mark.parametrize("dtype,hq,hkv,bs,n_q,lens", [
     ("bf16", 32, 8, 16, 16, [0, 16, 900, 2049]),            # 64 rows, pages of 16
     ("f16", 32, 8, 64, 24, [24, 25, 700, 1500]),            # 96 rows, pages of 64
     ("bf16", 16, 4, 1024, 30, [30, 1, 1100, 2050]),         # 120 rows, pages of 1024
     ("bf16", 32, 8, 4, 5, [5, 40, 333, 777]),               # 20 rows, pages of 4 (cp.async)
     ("f16", 32, 8, 32, 40, [40, 64, 500, 1600]),            # 160 rows, pages of 32: two Q tiles
+    ("bf16", 12, 3, 16, 8, [8, 0, 300, 1025, 77]),          # 32 rows, three kv heads
+    ("f16", 8, 8, 8, 48, [48, 49, 600]),                    # 48 rows (group 1)
+    ("bf16", 4, 1, 16, 12, [12, 500, 13]),                  # 48 rows, one kv head
 ])
 def test_pipelined_chunks_at_head_dim_128(lib, dtype, hq, hkv, bs, n_q, lens):
     pages = sum(-(-n // bs) for n in lens) + 5
