@@ -196,9 +196,11 @@ def test_chunk_of_64_rows_bad_page_zeroes_only_its_sequence(lib):
     assert_attn_close(out[1:], _ref(base, q, [1, 2]), base.dtype)
 
 
-def test_tensor_core_prefill(lib):
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f16", 64), ("bf16", 64)])
+def test_tensor_core_prefill(lib, dtype, d):
     # whole prompts: chunk_len == seq_len, so past == 0 and the read is causal prefill
-    base = workloads.make_batch("prefill", 43, "bf16", [200, 200, 200], 32, 8, 128, 16, 40)
+    # (head_dim 128: two Q tiles per CTA; head_dim 64: the pipelined one-tile read)
+    base = workloads.make_batch("prefill", 43, dtype, [200, 200, 200], 32, 8, d, 16, 40)
     q = _chunk_batch(base, 200)
     out = _run(lib, base, q)
     assert_attn_close(out, _ref(base, q), base.dtype, "prefill")

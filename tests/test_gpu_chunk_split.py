@@ -83,6 +83,8 @@ def _check_partials(po, pl, ref_po, ref_pl, dtype, what=""):
     ("bf16", 8, 8, 64, 16, 16, [16, 300, 900, 1111], 4),     # group 1: 16 queries, one head each
     ("bf16", 12, 3, 64, 16, 16, [16, 40, 3000, 1200, 5], 2),  # 64 rows, 15 (seq, kv head) pairs
     ("f16", 8, 1, 64, 16, 12, [12, 900, 1300], 9),           # 96 rows, one kv head
+    ("bf16", 32, 8, 64, 16, 100, [100, 110, 400], 4),        # 400 rows, a long chunk: one Q tile
+                                                             # per CTA at head_dim 64
 ])
 def test_partials_and_merge(lib, dtype, hq, hkv, d, bs, n_q, lens, pps):
     pages = sum(-(-n // bs) for n in lens) + 5
